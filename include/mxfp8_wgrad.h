@@ -1,0 +1,147 @@
+/*
+ * mxfp8_wgrad.h — C ABI of the GB300 (sm_103a) ragged MXFP8 weight-gradient
+ * grouped GEMM.
+ *
+ * The operation ("Ragged MXFP8 Weight Gradients: A FlyDSL Grouped GEMM on
+ * MI355X", section 1; "Group-GEMM in XLA", Part 3, "Contracting"):
+ *
+ *   for every expert g:  dW[g] = dY[g]^T . X[g]
+ *
+ * where the per-expert token offsets cut the CONTRACTION (token) axis. The
+ * operands arrive pre-quantised to MXFP8 along the token axis: A = dY^T [N,M]
+ * and B = X^T [K,M] hold E4M3 bytes with the token axis contiguous, and each
+ * run of 32 tokens of a row shares one E8M0 scale, stored in the row-major
+ * planes sA [N, M/32] and sB [K, M/32]. The output is dense bf16 [E,N,K]:
+ *
+ *   out[g,n,k] = bf16_rne( sum_{t in [lo_g, hi_g)} a(n,t) b(k,t) )
+ *   a(n,t) = e4m3(A[n,t]) * 2^(sA[n,t/32] - 127),  b likewise,
+ *   lo_0 = 0, lo_g = offs[g-1], hi_g = offs[g],
+ *
+ * accumulated in fp32 on the tensor cores and narrowed to bf16 with
+ * round-to-nearest-even (same page, section 5.5). Every output tile is owned
+ * by exactly one CTA for its whole reduction (same page, section 4): no
+ * atomics, no split-K, bit-reproducible output.
+ *
+ * Conventions for every entry point below:
+ *  - Pointers to operands, scales, offsets, outputs and workspaces are DEVICE
+ *    pointers owned by the caller; the library keeps none of them after the
+ *    call returns. All work is enqueued on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) and the call returns without synchronising.
+ *  - Layouts are dense row-major with no padding: A [N][M], B [K][M] (bytes),
+ *    sA [N][M/32], sB [K][M/32] (bytes), offs [E] (int32), out [E][N][K]
+ *    (bf16 bit patterns), x [R][M] (fp32).
+ *  - The return value is a status code (MXFP8_OK or a negative MXFP8_E*);
+ *    mxfp8_last_error() gives a message for the last failure on the calling
+ *    thread. Argument errors are detected on the host before anything is
+ *    enqueued. Errors the device detects (invalid offsets, a pipeline wait
+ *    that ran out) set bits of a device status word read by
+ *    mxfp8_device_status().
+ *  - Requires an sm_103 (GB300) or sm_100-family device with the library
+ *    built for it.
+ */
+#ifndef MXFP8_WGRAD_H
+#define MXFP8_WGRAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+#define MXFP8_OK 0
+#define MXFP8_EINVAL (-1)       /* null pointer, negative or zero size, M % 32 != 0, E too large */
+#define MXFP8_EALIGN (-2)       /* a pointer not 16-byte aligned, or K % 8 != 0 */
+#define MXFP8_ECUDA (-3)        /* a CUDA runtime/driver error (message attached) */
+#define MXFP8_EUNSUPPORTED (-4) /* the current device is not an sm_100-family GPU */
+#define MXFP8_ENOWS (-5)        /* caller workspace smaller than mxfp8_wgrad_workspace_bytes() */
+
+/* Bits of the device status word (mxfp8_device_status). */
+#define MXFP8_DEV_OFFS_UNSORTED 1   /* offs decreased somewhere; clamped to a non-decreasing sequence */
+#define MXFP8_DEV_OFFS_RANGE 2      /* an offset < 0 or > M; clamped into [0, M] */
+#define MXFP8_DEV_OFFS_ALIGN 4      /* an offset not a multiple of 32; rounded down */
+#define MXFP8_DEV_WAIT_TIMEOUT 8    /* a pipeline wait ran out; the CTA stopped and its tile is undefined */
+
+/* Largest expert count supported by one call. */
+#define MXFP8_MAX_EXPERTS 2048
+
+/*
+ * Ragged MXFP8 weight gradient ("Ragged MXFP8 Weight Gradients", section 1;
+ * operand layout A = dY^T [N,M], B = X^T [K,M], scale planes [N,M/32] and
+ * [K,M/32]; offs records where each expert's run of tokens ends).
+ *
+ *   A    [N][M]   E4M3 bytes, 16-byte aligned
+ *   sA   [N][M/32] E8M0 bytes
+ *   B    [K][M]   E4M3 bytes, 16-byte aligned
+ *   sB   [K][M/32] E8M0 bytes
+ *   offs [E]      int32 inclusive group ends. Preconditions (not checked on
+ *                 the host, which would need a synchronisation): non-decreasing,
+ *                 multiples of 32, offs[E-1] <= M. The device clamps violations
+ *                 into that form, so no access ever leaves the operands, and
+ *                 sets MXFP8_DEV_OFFS_* bits. Empty groups are allowed and give
+ *                 exact +0.0 slabs. Tokens in [offs[E-1], M) are never read
+ *                 into the contraction and may hold anything (NaN padding).
+ *   E    number of experts, 0 <= E <= MXFP8_MAX_EXPERTS (E == 0: no-op)
+ *   N, K output rows / columns, >= 1; K % 8 == 0
+ *   M    token count (columns of A and B), M % 32 == 0, M >= 32
+ *   out  [E][N][K] bf16, 16-byte aligned; every element is written
+ *   stream cudaStream_t
+ *
+ * Scratch space (the scale re-layout and the schedule) comes from a cache the
+ * library keeps per (device, stream), grown with stream-ordered allocation and
+ * reused across calls; calls on one stream are ordered, so they never share
+ * scratch concurrently.
+ */
+int mxfp8_wgrad_grouped(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                        const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
+                        void* stream);
+
+/* Bytes of scratch that mxfp8_wgrad_grouped_ws needs for these sizes (an upper
+ * bound over every routing of M tokens into E groups). 0 if the sizes are
+ * invalid. Host-only, no CUDA call. */
+size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M);
+
+/* As mxfp8_wgrad_grouped, with caller-provided scratch: `workspace` is a
+ * device pointer, 256-byte aligned, of at least
+ * mxfp8_wgrad_workspace_bytes(E,N,K,M) bytes (else MXFP8_ENOWS). The
+ * workspace must not be used by any other work until this call's kernels have
+ * finished on `stream`. */
+int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                           const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Tokenwise MXFP8 quantiser, used to build operands ("Ragged MXFP8 Weight
+ * Gradients", section 1: one E8M0 scale per 32 elements along the token axis).
+ * For each row r and each 32-token block b with amax = max |x| over the block:
+ *   e = the smallest integer with amax <= 448 * 2^e (the scale 2^ceil(log2(amax/448))),
+ *       clamped to [-127, 127]; amax == 0 gives e = -127;
+ *   s[r][b] = e + 127 (E8M0);
+ *   q[r][t] = E4M3(x[r][t] * 2^-e), round to nearest even, saturating at +-448.
+ * A block holding a NaN or an infinity gets s = 0xFF and q = 0x7F (NaN).
+ *   x [R][M] fp32 (16-byte aligned), q [R][M] bytes (8-byte aligned),
+ *   s [R][M/32] bytes; R >= 1, M >= 32, M % 32 == 0.
+ */
+int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, void* stream);
+
+/* Message for the last non-zero status returned on the calling thread
+ * (thread-local; never NULL). */
+const char* mxfp8_last_error(void);
+
+/* Reads the device status word of the current device into *status (a
+ * combination of MXFP8_DEV_* bits; 0 when nothing was flagged) and, if
+ * `clear` is non-zero, resets it. Synchronises the current device first. */
+int mxfp8_device_status(int32_t* status, int clear);
+
+/* Measurement hook: when both events are non-NULL, the next
+ * mxfp8_wgrad_grouped{,_ws} call on this thread records `ev_before` on its
+ * stream right before the main contraction kernel and `ev_after` right after
+ * it (cudaEvent_t handles). The hook is consumed by that one call. */
+int mxfp8_wgrad_set_timing_events(void* ev_before, void* ev_after);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_WGRAD_H */

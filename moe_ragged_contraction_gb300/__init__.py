@@ -1,0 +1,20 @@
+"""GB300-native ragged MXFP8 MoE weight-gradient grouped GEMM.
+
+dW[g] = dY[g]^T X[g] for every expert g, where per-expert token offsets cut
+the contraction axis ("Ragged MXFP8 Weight Gradients: A FlyDSL Grouped GEMM on
+MI355X", section 1), computed by hand-written sm_103a CUDA kernels (TMA,
+tcgen05 block-scaled MMA, TMEM) behind the C ABI in ``include/mxfp8_wgrad.h``.
+
+The Python API below is a thin ctypes binding: argument marshalling only.
+"""
+from ._lib import (  # noqa: F401
+    Mxfp8Error,
+    device_status,
+    lib_path,
+    load,
+    quantize_tokenwise,
+    set_timing_events,
+    wgrad_grouped,
+    workspace_bytes,
+)
+from .build import build  # noqa: F401

@@ -1,0 +1,169 @@
+"""ctypes binding of ``libmxfp8_wgrad.so`` (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only turns torch tensors into device pointers, sizes and the current stream.
+There is no fallback: if the library is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+EINVAL = -1
+EALIGN = -2
+ECUDA = -3
+EUNSUPPORTED = -4
+ENOWS = -5
+
+DEV_OFFS_UNSORTED = 1
+DEV_OFFS_RANGE = 2
+DEV_OFFS_ALIGN = 4
+DEV_WAIT_TIMEOUT = 8
+
+
+class Mxfp8Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(
+                f"CUDA library {path} is missing: build it with "
+                "`python -m moe_ragged_contraction_gb300.build` (or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        P, I, L, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        lib.mxfp8_wgrad_grouped.argtypes = [P, P, P, P, P, I, I, I, L, P, P]
+        lib.mxfp8_wgrad_grouped.restype = I
+        lib.mxfp8_wgrad_workspace_bytes.argtypes = [I, I, I, L]
+        lib.mxfp8_wgrad_workspace_bytes.restype = Z
+        lib.mxfp8_wgrad_grouped_ws.argtypes = [P, P, P, P, P, I, I, I, L, P, P, Z, P]
+        lib.mxfp8_wgrad_grouped_ws.restype = I
+        lib.mxfp8_quantize_tokenwise.argtypes = [P, I, L, P, P, P]
+        lib.mxfp8_quantize_tokenwise.restype = I
+        lib.mxfp8_last_error.argtypes = []
+        lib.mxfp8_last_error.restype = ctypes.c_char_p
+        lib.mxfp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), I]
+        lib.mxfp8_device_status.restype = I
+        lib.mxfp8_wgrad_set_timing_events.argtypes = [P, P]
+        lib.mxfp8_wgrad_set_timing_events.restype = I
+        _lib = lib
+        return lib
+
+
+def check(rc: int) -> None:
+    if rc != OK:
+        msg = load().mxfp8_last_error().decode(errors="replace")
+        raise Mxfp8Error(rc, msg)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _expect(t, dtype, name, device=True):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def wgrad_grouped(A, sA, B, sB, offs, out=None, workspace=None, stream=None):
+    """dW[g] = dY[g]^T X[g] for every expert (see include/mxfp8_wgrad.h).
+
+    A: uint8 [N, M] (E4M3), sA: uint8 [N, M/32] (E8M0), B: uint8 [K, M],
+    sB: uint8 [K, M/32], offs: int32 [E] inclusive group ends (device).
+    Returns (or fills) ``out``: bf16 [E, N, K].
+    """
+    import torch
+
+    for t, dt, nm in ((A, torch.uint8, "A"), (sA, torch.uint8, "sA"), (B, torch.uint8, "B"),
+                      (sB, torch.uint8, "sB"), (offs, torch.int32, "offs")):
+        _expect(t, dt, nm)
+    N, M = A.shape
+    K, M2 = B.shape
+    E = offs.numel()
+    if M2 != M or tuple(sA.shape) != (N, M // 32) or tuple(sB.shape) != (K, M // 32):
+        raise ValueError("inconsistent operand / scale shapes")
+    if out is None:
+        out = torch.empty((E, N, K), dtype=torch.bfloat16, device=A.device)
+    _expect(out, torch.bfloat16, "out")
+    if tuple(out.shape) != (E, N, K):
+        raise ValueError(f"out must be [{E}, {N}, {K}]")
+    lib = load()
+    if workspace is None:
+        rc = lib.mxfp8_wgrad_grouped(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offs), E, N, K, M,
+                                     _ptr(out), _stream(stream))
+    else:
+        _expect(workspace, torch.uint8, "workspace")
+        rc = lib.mxfp8_wgrad_grouped_ws(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offs), E, N, K, M,
+                                        _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    check(rc)
+    return out
+
+
+def workspace_bytes(E: int, N: int, K: int, M: int) -> int:
+    return int(load().mxfp8_wgrad_workspace_bytes(E, N, K, M))
+
+
+def quantize_tokenwise(x, q=None, s=None, stream=None):
+    """Tokenwise MXFP8 quantiser: x fp32 [R, M] -> (q uint8 [R, M], s uint8 [R, M/32])."""
+    import torch
+
+    _expect(x, torch.float32, "x")
+    R, M = x.shape
+    if q is None:
+        q = torch.empty((R, M), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((R, M // 32), dtype=torch.uint8, device=x.device)
+    _expect(q, torch.uint8, "q")
+    _expect(s, torch.uint8, "s")
+    check(load().mxfp8_quantize_tokenwise(_ptr(x), R, M, _ptr(q), _ptr(s), _stream(stream)))
+    return q, s
+
+
+def device_status(clear: bool = True) -> int:
+    """Device status word (DEV_* bits); synchronises the current device."""
+    v = ctypes.c_int32(0)
+    check(load().mxfp8_device_status(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
+
+
+def set_timing_events(ev_before, ev_after) -> None:
+    """Record torch.cuda.Event pair around the main kernel of the next call."""
+    b = ctypes.c_void_p(ev_before.cuda_event) if ev_before is not None else None
+    a = ctypes.c_void_p(ev_after.cuda_event) if ev_after is not None else None
+    check(load().mxfp8_wgrad_set_timing_events(b, a))

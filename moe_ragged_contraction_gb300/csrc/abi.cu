@@ -1,0 +1,259 @@
+// C ABI of the library: argument validation, tensor-map creation, the
+// per-(device, stream) scratch cache, and status / error reporting.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <vector>
+
+#include "mxw_internal.h"
+#include "../../include/mxfp8_wgrad.h"
+
+namespace {
+
+thread_local char g_err[512] = "no error";
+thread_local cudaEvent_t g_ev_before = nullptr;
+thread_local cudaEvent_t g_ev_after = nullptr;
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+    return fail(MXFP8_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+    bool valid = false;
+    int major = 0, minor = 0, sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Device checks: an sm_100-family GPU with the library's sm_103a build.
+int current_device(int* dev, DeviceInfo* info) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= 64) return fail(MXFP8_EUNSUPPORTED, "device index %d out of range", *dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[*dev];
+    if (!d.valid) {
+        e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, *dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, *dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+        d.valid = true;
+    }
+    *info = d;
+    if (d.major != 10 || d.minor != 3)
+        return fail(MXFP8_EUNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", *dev,
+                    d.major, d.minor);
+    return MXFP8_OK;
+}
+
+int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            return fail(MXFP8_ECUDA, "cuTensorMapEncodeTiled entry point unavailable (%s)", cudaGetErrorString(e));
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    *fn = g_encode;
+    return MXFP8_OK;
+}
+
+// Token-contiguous E4M3 operand [rows][M] -> box of box_rows rows x 128 tokens,
+// 128-byte swizzle; out-of-range rows and tokens read as zero.
+int make_operand_map(CUtensorMap* map, const uint8_t* base, int rows, int64_t M, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encoder(&enc);
+    if (rc) return rc;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(M)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mxw::BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MXFP8_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return MXFP8_OK;
+}
+
+// Scratch cache keyed by (device, stream). Growth frees the old block in
+// stream order and allocates the new one in stream order, so earlier calls
+// on the same stream finish with the old block first.
+struct WsEntry {
+    int dev;
+    cudaStream_t stream;
+    void* ptr;
+    size_t bytes;
+};
+std::vector<WsEntry> g_ws;
+
+int cached_workspace(int dev, cudaStream_t stream, size_t need, void** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (WsEntry& w : g_ws) {
+        if (w.dev == dev && w.stream == stream) {
+            if (w.bytes >= need) {
+                *out = w.ptr;
+                return MXFP8_OK;
+            }
+            cudaError_t e = cudaFreeAsync(w.ptr, stream);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaFreeAsync (workspace)");
+            w.ptr = nullptr;
+            w.bytes = 0;
+            e = cudaMallocAsync(&w.ptr, need, stream);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (workspace)");
+            w.bytes = need;
+            *out = w.ptr;
+            return MXFP8_OK;
+        }
+    }
+    WsEntry w{dev, stream, nullptr, 0};
+    cudaError_t e = cudaMallocAsync(&w.ptr, need, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (workspace)");
+    w.bytes = need;
+    g_ws.push_back(w);
+    *out = w.ptr;
+    return MXFP8_OK;
+}
+
+uint64_t wait_limit_ns() {
+    static uint64_t v = [] {
+        const char* s = getenv("MXFP8_WAIT_LIMIT_MS");
+        long long ms = s ? atoll(s) : 1000;
+        if (ms < 1) ms = 1;
+        if (ms > 60000) ms = 60000;
+        return static_cast<uint64_t>(ms) * 1000000ull;
+    }();
+    return v;
+}
+
+int validate(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const int32_t* offs, int E,
+             int N, int K, int64_t M, const uint16_t* out) {
+    if (E < 0 || E > MXFP8_MAX_EXPERTS) return fail(MXFP8_EINVAL, "E=%d out of range [0, %d]", E, MXFP8_MAX_EXPERTS);
+    if (N < 1 || K < 1) return fail(MXFP8_EINVAL, "N=%d and K=%d must be >= 1", N, K);
+    if (M < 32 || (M % 32) != 0) return fail(MXFP8_EINVAL, "M=%lld must be a positive multiple of 32", (long long)M);
+    if (M > (int64_t(1) << 31) - 256) return fail(MXFP8_EINVAL, "M=%lld too large", (long long)M);
+    if (E == 0) return MXFP8_OK;
+    if (!A || !sA || !B || !sB || !offs || !out) return fail(MXFP8_EINVAL, "null pointer argument");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out))
+        return fail(MXFP8_EALIGN, "A, B and out must be 16-byte aligned");
+    if ((K % 8) != 0) return fail(MXFP8_EALIGN, "K=%d must be a multiple of 8 (16-byte output rows)", K);
+    return MXFP8_OK;
+}
+
+int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const int32_t* offs, int E, int N,
+        int K, int64_t M, uint16_t* out, void* ws, size_t ws_bytes, bool use_cache, void* stream) {
+    cudaEvent_t evb = g_ev_before, eva = g_ev_after;
+    g_ev_before = g_ev_after = nullptr;
+    int rc = validate(A, sA, B, sB, offs, E, N, K, M, out);
+    if (rc) return rc;
+    if (E == 0) return MXFP8_OK;
+    mxw::WsLayout lay;
+    if (!mxw::ws_layout(E, N, K, M, &lay)) return fail(MXFP8_EINVAL, "unsupported sizes");
+    if (!use_cache) {
+        if (!ws) return fail(MXFP8_EINVAL, "null workspace");
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MXFP8_EALIGN, "workspace must be 256-byte aligned");
+        if (ws_bytes < lay.total)
+            return fail(MXFP8_ENOWS, "workspace of %zu bytes, need %zu", ws_bytes, lay.total);
+    }
+    int dev;
+    DeviceInfo info;
+    rc = current_device(&dev, &info);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (use_cache) {
+        rc = cached_workspace(dev, st, lay.total, &ws);
+        if (rc) return rc;
+    }
+    CUtensorMap mapA, mapB;
+    rc = make_operand_map(&mapA, A, N, M, mxw::BM);
+    if (rc) return rc;
+    rc = make_operand_map(&mapB, B, K, M, mxw::BN);
+    if (rc) return rc;
+
+    mxw::WgradArgs a;
+    a.A = A; a.sA = sA; a.B = B; a.sB = sB; a.offs = offs;
+    a.E = E; a.N = N; a.K = K; a.M = M; a.out = out;
+    a.ws = static_cast<uint8_t*>(ws);
+    a.lay = lay;
+    a.dev = dev;
+    a.num_sms = info.sms;
+    a.wait_limit_ns = wait_limit_ns();
+    a.stream = st;
+    a.ev_before = evb;
+    a.ev_after = eva;
+    const char* what = "";
+    cudaError_t e = mxw::launch_wgrad(a, mapA, mapB, &what);
+    if (e != cudaSuccess) return fail_cuda(e, what);
+    return MXFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp8_wgrad_grouped(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                        const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out, void* stream) {
+    return run(A, sA, B, sB, offs, E, N, K, M, out, nullptr, 0, true, stream);
+}
+
+size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M) {
+    mxw::WsLayout lay;
+    if (!mxw::ws_layout(E, N, K, M, &lay)) return 0;
+    return lay.total;
+}
+
+int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                           const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    return run(A, sA, B, sB, offs, E, N, K, M, out, workspace, workspace_bytes, false, stream);
+}
+
+int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, void* stream) {
+    if (R < 1) return fail(MXFP8_EINVAL, "R=%d must be >= 1", R);
+    if (M < 32 || (M % 32) != 0) return fail(MXFP8_EINVAL, "M=%lld must be a positive multiple of 32", (long long)M);
+    if (!x || !q || !s) return fail(MXFP8_EINVAL, "null pointer argument");
+    if (!aligned16(x)) return fail(MXFP8_EALIGN, "x must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(q) & 7u) != 0) return fail(MXFP8_EALIGN, "q must be 8-byte aligned");
+    int dev;
+    DeviceInfo info;
+    int rc = current_device(&dev, &info);
+    if (rc) return rc;
+    cudaError_t e = mxw::launch_quantize(x, R, M, q, s, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "quantize kernel");
+    return MXFP8_OK;
+}
+
+const char* mxfp8_last_error(void) { return g_err; }
+
+int mxfp8_device_status(int32_t* status, int clear) {
+    if (!status) return fail(MXFP8_EINVAL, "null status pointer");
+    cudaError_t e = mxw::read_device_status(status, clear);
+    if (e != cudaSuccess) return fail_cuda(e, "device status");
+    return MXFP8_OK;
+}
+
+int mxfp8_wgrad_set_timing_events(void* ev_before, void* ev_after) {
+    if ((ev_before == nullptr) != (ev_after == nullptr))
+        return fail(MXFP8_EINVAL, "give both timing events or neither");
+    g_ev_before = static_cast<cudaEvent_t>(ev_before);
+    g_ev_after = static_cast<cudaEvent_t>(ev_after);
+    return MXFP8_OK;
+}
+
+}  // extern "C"

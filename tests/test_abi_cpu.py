@@ -1,0 +1,100 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads without
+a GPU, exports every function include/*.h declares, and rejects invalid
+arguments on the host (no compute call is made here)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import moe_ragged_contraction_gb300 as mx
+from moe_ragged_contraction_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mx.build()
+    return mx.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mxfp8_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("mxfp8_wgrad_grouped", "mxfp8_quantize_tokenwise", "mxfp8_wgrad_grouped_ws",
+              "mxfp8_wgrad_workspace_bytes", "mxfp8_last_error", "mxfp8_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_workspace_bytes(lib):
+    f = lib.mxfp8_wgrad_workspace_bytes
+    assert f(0, 128, 256, 1024) == 0
+    assert f(4, 128, 256, 1000) == 0  # M % 32 != 0
+    assert f(4, 128, 256, 1024) > 0
+    # grows with tokens, rows and columns
+    assert f(8, 1408, 2048, 65536) > f(8, 1408, 2048, 32768) > f(8, 128, 2048, 32768)
+
+
+P = 0x10000  # 16-byte aligned fake address: never dereferenced on these paths
+
+
+def call(lib, A=P, sA=P, B=P, sB=P, offs=P, E=4, N=128, K=256, M=1024, out=P):
+    return lib.mxfp8_wgrad_grouped(A, sA, B, sB, offs, E, N, K, M, out, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=-1), _lib.EINVAL), (dict(E=100000), _lib.EINVAL), (dict(N=0), _lib.EINVAL),
+    (dict(K=0), _lib.EINVAL), (dict(M=1000), _lib.EINVAL), (dict(M=0), _lib.EINVAL),
+    (dict(A=None), _lib.EINVAL), (dict(offs=None), _lib.EINVAL), (dict(out=None), _lib.EINVAL),
+    (dict(A=P + 8), _lib.EALIGN), (dict(out=P + 4), _lib.EALIGN), (dict(K=260), _lib.EALIGN),
+])
+def test_host_validation(lib, kw, code):
+    assert call(lib, **kw) == code
+    assert len(lib.mxfp8_last_error()) > 0
+
+
+def test_empty_expert_count_is_noop(lib):
+    assert call(lib, E=0, A=None, sA=None, B=None, sB=None, offs=None, out=None) == _lib.OK
+
+
+def test_ws_variant_checks_size(lib):
+    need = lib.mxfp8_wgrad_workspace_bytes(4, 128, 256, 1024)
+    rc = lib.mxfp8_wgrad_grouped_ws(P, P, P, P, P, 4, 128, 256, 1024, P, P, need - 1, None)
+    assert rc == _lib.ENOWS
+    rc = lib.mxfp8_wgrad_grouped_ws(P, P, P, P, P, 4, 128, 256, 1024, P, P + 16, need, None)
+    assert rc == _lib.EALIGN  # workspace needs 256-byte alignment
+
+
+def test_quantize_validation(lib):
+    q = lib.mxfp8_quantize_tokenwise
+    assert q(P, 0, 1024, P, P, None) == _lib.EINVAL
+    assert q(P, 4, 1000, P, P, None) == _lib.EINVAL
+    assert q(None, 4, 1024, P, P, None) == _lib.EINVAL
+    assert q(P + 4, 4, 1024, P, P, None) == _lib.EALIGN
+
+
+def test_timing_events_pairing(lib):
+    assert lib.mxfp8_wgrad_set_timing_events(ctypes.c_void_p(P), None) == _lib.EINVAL
+    assert lib.mxfp8_wgrad_set_timing_events(None, None) == _lib.OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib._build, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.load()

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: bit-exact on exactly-representable cases and on the quantiser; within
+|gpu - oracle| <= 1e-2 |oracle| + 1e-3 sqrt(sum |a b|) elsewhere;
+bit-reproducible run to run; every output element written (NaN-poisoned
+outputs); padding past the last group never read into the result; empty
+experts exact +0.0."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_ragged_contraction_gb300 as mx
+from moe_ragged_contraction_gb300 import inputs as I
+
+from _util import (quantised_operand, same_bits_signless_zero, tolerance_violations)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mx.build()
+    mx.load()
+    mx.device_status(clear=True)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_gpu(A, sA, B, sB, offs, E, N, K, poison=True, workspace=None):
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    if poison:
+        out.view(torch.int16).fill_(-1)  # 0xFFFF: bf16 NaN, so an unwritten element shows
+    mx.wgrad_grouped(dev(A), dev(sA), dev(B), dev(sB), dev(np.asarray(offs, np.int32)), out=out,
+                     workspace=workspace)
+    torch.cuda.synchronize()
+    return out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rand_operand(rng, R, M, scale_lo=118, scale_hi=136):
+    q = rng.integers(0, 256, size=(R, M), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x7E
+    s = rng.integers(scale_lo, scale_hi, size=(R, M // 32), dtype=np.uint8)
+    return q, s
+
+
+def check_tol(got, A, sA, B, sB, offs, E, N, K, M):
+    ref, acc, aacc = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
+    bad = tolerance_violations(got, ref, aacc)
+    assert not bad.any(), f"{bad.sum()} of {bad.size} elements out of tolerance; first at {np.argwhere(bad)[:5].tolist()}"
+    lo = 0
+    for g in range(E):
+        if int(offs[g]) == lo:
+            assert np.all(got[g] == 0x0000), f"empty expert {g} not exact +0"
+        lo = int(offs[g])
+    return ref
+
+
+# ------------------------------------------------------------------ quantiser
+
+@pytest.mark.parametrize("R,M,dist", [(128, 1024, "normal"), (37, 4096, "student_t3"), (1, 32, "normal")])
+def test_quantiser_bit_exact(R, M, dist):
+    x = I.host_operand(R, M, seed=77, stream=0, dist=dist)
+    x[:, :32] *= np.float32(1e-30)  # tiny values: subnormal E4M3 codes
+    if R > 2:
+        x[1, 64:96] = 0.0
+        x[2, 0:32] = np.float32(448.0 * 2.0 ** 5)
+    q_ref, s_ref = oracle.quantize_tokenwise(x)
+    q, s = mx.quantize_tokenwise(dev(x))
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_quantiser_nonfinite():
+    x = np.ones((2, 64), np.float32)
+    x[0, 3] = np.nan
+    x[1, 40] = -np.inf
+    q_ref, s_ref = oracle.quantize_tokenwise(x)
+    q, s = mx.quantize_tokenwise(dev(x))
+    assert np.array_equal(s.cpu().numpy(), s_ref) and np.array_equal(q.cpu().numpy(), q_ref)
+
+
+# ------------------------------------------------------------------ exact cases
+
+def int_operand(rng, R, M, vals, codes):
+    v = rng.choice(vals, size=(R, M))
+    return np.vectorize(codes.get)(v).astype(np.uint8)
+
+
+def test_exact_tier1_integers_unit_scales():
+    """Values in [-2, 2], unit scales, groups <= 1024 tokens: every partial sum
+    is an integer below 2^12, so any fp32 accumulation order is exact."""
+    rng = np.random.default_rng(1)
+    codes = {-2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40}
+    E, N, K, M = 5, 256, 512, 2048
+    A = int_operand(rng, N, M, list(codes), codes)
+    B = int_operand(rng, K, M, list(codes), codes)
+    sA = np.full((N, M // 32), 0x7F, np.uint8)
+    sB = np.full((K, M // 32), 0x7F, np.uint8)
+    offs = np.cumsum([0, 416, 1024, 96, 480]).astype(np.int32)  # one empty, 32-aligned, ragged
+    got = run_gpu(A, sA, B, sB, offs, E, N, K)
+    ref = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M)
+    assert same_bits_signless_zero(got, ref)
+    assert np.all(got[0] == 0)
+
+
+def test_exact_tier2_scaled_integers():
+    """Integers in [-16, 16] (E4M3-exact) with per-block scales 2^[-2, 2]:
+    products are multiples of 2^-4 and |sums| < 2^20, exact in fp32."""
+    rng = np.random.default_rng(2)
+    vals = list(range(-16, 17))
+    t = torch.tensor(np.array(vals, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    codes = dict(zip(vals, t.tolist()))
+    E, N, K, M = 3, 128, 256, 1024
+    A = int_operand(rng, N, M, vals, codes)
+    B = int_operand(rng, K, M, vals, codes)
+    sA = rng.integers(125, 130, size=(N, M // 32), dtype=np.uint8)
+    sB = rng.integers(125, 130, size=(K, M // 32), dtype=np.uint8)
+    offs = np.array([320, 640, 1024], np.int32)
+    got = run_gpu(A, sA, B, sB, offs, E, N, K)
+    ref, acc, _ = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
+    assert np.all(np.abs(acc) < 2.0 ** 20)
+    assert same_bits_signless_zero(got, ref), f"{np.sum(got != ref)} elements differ"
+
+
+# ------------------------------------------------------------------ tolerance parity
+
+def test_tiny_workload_full():
+    w = I.WORKLOADS["tiny"]
+    A, sA = quantised_operand(w.N, w.M, w.seed, 0, w.dist)
+    B, sB = quantised_operand(w.K, w.M, w.seed, 1, w.dist)
+    offs = I.offsets(I.group_sizes("tiny"))
+    got = run_gpu(A, sA, B, sB, offs, w.E, w.N, w.K)
+    check_tol(got, A, sA, B, sB, offs, w.E, w.N, w.K, w.M)
+
+
+@pytest.mark.parametrize("E,N,K,M,sizes", [
+    (1, 128, 256, 128, [128]),                        # one tile, one K-step
+    (1, 128, 256, 96, [96]),                          # single partial K-step
+    (2, 128, 256, 256, [32, 224]),                    # 32-token group, boundary mid K-step
+    (3, 320, 640, 1536, [608, 0, 928]),               # N, K not tile multiples
+    (4, 1408, 1152, 2048, [800, 352, 0, 896]),        # 11 row tiles, K = 4.5 col tiles
+    (1, 40, 8, 512, [512]),                           # tiny N and K
+    (2, 256, 256, 4096, [4064, 32]),                  # long group, then a 32-token group
+    (3, 128, 256, 1024, [0, 0, 0]),                   # all experts empty
+    (64, 128, 256, 4096, None),                       # many experts, small groups
+])
+def test_edge_shapes(E, N, K, M, sizes):
+    rng = np.random.default_rng(E * 1000 + N + K + M)
+    A, sA = rand_operand(rng, N, M)
+    B, sB = rand_operand(rng, K, M)
+    if sizes is None:
+        sizes = I.random_sizes(E, M, rng)
+    offs = np.cumsum(sizes).astype(np.int32)
+    got = run_gpu(A, sA, B, sB, offs, E, N, K)
+    check_tol(got, A, sA, B, sB, offs, E, N, K, M)
+
+
+def test_varied_scales_move_rows_and_columns():
+    """Scales that vary per (row, 32-token block) on both operands: a misplaced
+    scale would shift whole rows or columns, far outside the tolerance."""
+    rng = np.random.default_rng(31)
+    E, N, K, M = 2, 256, 512, 1024
+    A, sA = rand_operand(rng, N, M, 110, 145)
+    B, sB = rand_operand(rng, K, M, 110, 145)
+    offs = np.array([480, 1024], np.int32)
+    got = run_gpu(A, sA, B, sB, offs, E, N, K)
+    check_tol(got, A, sA, B, sB, offs, E, N, K, M)
+
+
+# ------------------------------------------------------------------ properties
+
+def test_bit_reproducible_and_workspace_variant():
+    rng = np.random.default_rng(41)
+    E, N, K, M = 6, 384, 768, 3072
+    A, sA = rand_operand(rng, N, M)
+    B, sB = rand_operand(rng, K, M)
+    offs = np.cumsum(I.random_sizes(E, M, rng)).astype(np.int32)
+    runs = [run_gpu(A, sA, B, sB, offs, E, N, K) for _ in range(3)]
+    assert all(np.array_equal(runs[0], r) for r in runs[1:])
+    ws = torch.empty(mx.workspace_bytes(E, N, K, M), dtype=torch.uint8, device="cuda")
+    assert np.array_equal(runs[0], run_gpu(A, sA, B, sB, offs, E, N, K, workspace=ws))
+
+
+def test_padding_garbage_never_read():
+    """NaN data and NaN scales past the last group give the same bits as the
+    same call on operands cut down to their real token width."""
+    rng = np.random.default_rng(51)
+    E, N, K, M = 3, 256, 512, 2048
+    A, sA = rand_operand(rng, N, M)
+    B, sB = rand_operand(rng, K, M)
+    offs = np.array([416, 416, 1376], np.int32)
+    Mc = int(offs[-1])
+    cut = run_gpu(A[:, :Mc].copy(), sA[:, :Mc // 32].copy(), B[:, :Mc].copy(), sB[:, :Mc // 32].copy(),
+                  offs, E, N, K)
+    A2, sA2, B2, sB2 = A.copy(), sA.copy(), B.copy(), sB.copy()
+    A2[:, Mc:] = 0x7F; B2[:, Mc:] = 0xFF
+    sA2[:, Mc // 32:] = 0xFF; sB2[:, Mc // 32:] = 0xFF
+    got = run_gpu(A2, sA2, B2, sB2, offs, E, N, K)
+    assert np.array_equal(got, cut)
+    check_tol(got, A, sA, B, sB, offs, E, N, K, M)
+
+
+def test_invalid_offsets_are_clamped_and_flagged():
+    rng = np.random.default_rng(61)
+    E, N, K, M = 4, 128, 256, 1024
+    A, sA = rand_operand(rng, N, M)
+    B, sB = rand_operand(rng, K, M)
+    mx.device_status(clear=True)
+    bad = np.array([300, 200, 5000, 1024], np.int32)  # unaligned, decreasing, beyond M
+    got = run_gpu(A, sA, B, sB, bad, E, N, K)
+    st = mx.device_status(clear=True)
+    assert st & 1 and st & 2 and st & 4 and not st & 8
+    clamped = np.array([288, 288, 1024, 1024], np.int32)
+    check_tol(got, A, sA, B, sB, clamped, E, N, K, M)
+    assert mx.device_status(clear=True) == 0
