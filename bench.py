@@ -1,0 +1,412 @@
+"""Benchmark: ragged MXFP8 weight-gradient grouped GEMM on GB300.
+
+One step = one full call of the hot path (plan + scale re-layout kernel and
+the main tcgen05 contraction kernel) over one batch of synthetic input that is
+already resident in HBM; the L2 is flushed (a 256 MiB write) before every
+timed step, outside the timed interval. Quantisation builds the inputs and is
+not timed ("Ragged MXFP8 Weight Gradients", section 7: operator time on
+pre-quantised operands).
+
+Metric: TFLOP/s = 2 N K sum_g len_g / time. Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 16B] [--impl reference]
+
+--impl reference times the CPU oracle (the plain fp64 definition) on the
+host's cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from moe_ragged_contraction_gb300 import inputs as I  # noqa: E402
+
+DEFAULT_CONFIG = "16B"
+METRIC = "TFLOP/s (2*N*K*sum(M_g)) ragged MXFP8 wgrad, % of GB300 MXFP8 tensor peak"
+FP8_OVER_BF16 = 2.0  # nominal dense ratio: 4.5 PF fp8 / 2.25 PF bf16
+L2_FLUSH_BYTES = 256 << 20
+MAIN_KERNEL_SRC = os.path.join(ROOT, "moe_ragged_contraction_gb300", "csrc", "wgrad_kernels.cu")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.dirname(MAIN_KERNEL_SRC))):
+        with open(os.path.join(os.path.dirname(MAIN_KERNEL_SRC), f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def mxfp8_peak():
+    """Dense MXFP8 peak in TFLOP/s: the measured bf16 burst peak x the nominal
+    fp8/bf16 ratio (measured file), else the fallback figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        return FP8_OVER_BF16 * float(mp["bf16_tflops"]), "measured bf16 burst x2 (nominal fp8/bf16)", mp
+    except (OSError, KeyError, ValueError):
+        return FP8_OVER_BF16 * 1900.0, "fallback 1.9 PF bf16 x2 (nominal fp8/bf16)", None
+
+
+def measured_traffic(config: str):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    or None if the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = t.get(config)
+    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append((float(p[1]), float(p[2]), p[5], p[6], p[7], p[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for nm, v in zip(names, r[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def make_device_inputs(name: str, device):
+    """Seeded fp32 operands generated on the GPU, quantised by the library's
+    tokenwise quantiser (input building; not timed)."""
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    w = I.WORKLOADS[name]
+    ops = []
+    for stream, rows in ((0, w.N), (1, w.K)):
+        q = torch.empty((rows, w.M), dtype=torch.uint8, device=device)
+        s = torch.empty((rows, w.M // 32), dtype=torch.uint8, device=device)
+        step = max(1, (1 << 30) // (4 * w.M))  # <= 1 GiB of fp32 at a time
+        for r0 in range(0, rows, step):
+            r1 = min(rows, r0 + step)
+            x = I.device_operand(r1 - r0, w.M, w.seed * 7919 + r0, stream, w.dist, device=device)
+            mx.quantize_tokenwise(x, q[r0:r1], s[r0:r1])
+            del x
+        ops += [q, s]
+    offs = torch.from_numpy(I.offsets(I.group_sizes(name))).to(device)
+    torch.cuda.synchronize()
+    return ops[0], ops[1], ops[2], ops[3], offs
+
+
+def cpu_oracle_rate(A, sA, B, sB, offs, w, target_s: float, threads: int, seed: int = 0):
+    """Time the oracle on a bounded sample: whole output rows (all K columns)
+    of every non-empty expert, as many rows as fit ~target_s seconds.
+    Returns (TFLOP/s, seconds, description)."""
+    import oracle
+
+    sizes = np.diff(np.concatenate([[0], offs]))
+    live = np.nonzero(sizes > 0)[0]
+    rng = np.random.default_rng(seed)
+
+    def sample(rows_per_expert):
+        gs, ns, ks = [], [], []
+        for g in live:
+            for n in rng.integers(0, w.N, rows_per_expert):
+                gs.append(np.full(w.K, g)); ns.append(np.full(w.K, n)); ks.append(np.arange(w.K))
+        return (np.concatenate(gs).astype(np.int32), np.concatenate(ns).astype(np.int32),
+                np.concatenate(ks).astype(np.int32))
+
+    def run(rows):
+        g, n, k = sample(rows)
+        flop = 2.0 * float(np.sum(sizes[g]))
+        t0 = time.perf_counter()
+        oracle.wgrad_points(A, sA, B, sB, offs, w.E, w.N, w.K, w.M, g, n, k, nthreads=threads)
+        return flop, time.perf_counter() - t0
+
+    flop, dt = run(1)  # calibration
+    rows = int(max(1, min(w.N, round(target_s / max(dt, 1e-6)))))
+    if rows > 1:
+        flop, dt = run(rows)
+    desc = (f"{rows} random full output row(s) (all {w.K} columns) of each of the {len(live)} non-empty experts, "
+            f"{flop / 2:.3g} MACs")
+    return flop / dt / 1e12, dt, desc
+
+
+def bench_gpu(args):
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    mx.build()
+    mx.load()
+
+    w = I.WORKLOADS[args.config]
+    A, sA, B, sB, offs = make_device_inputs(args.config, device)
+    out = torch.empty((w.E, w.N, w.K), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(main_pair=None):
+        if main_pair is not None:
+            mx.set_timing_events(*main_pair)
+        mx.wgrad_grouped(A, sA, B, sB, offs, out=out)
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = str(torch.cuda.current_device())
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    # warm-up: W steps, then ~0.5 s of back-to-back calls so clocks settle
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in evm:  # torch creates the CUDA event on first record; the library needs real handles
+        a.record(stream)
+        b.record(stream)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(main_pair=evm[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    main_ms = [a.elapsed_time(b) for a, b in evm]
+    total_ms = float(np.sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert mx.device_status(clear=True) == 0, "device flagged an error during the benchmark"
+
+    # end to end through the public API with host buffers: H2D of every input,
+    # the call, D2H of the output, all inside the timed interval
+    hA, hsA, hB, hsB, hoffs = (t.cpu().pin_memory() for t in (A, sA, B, sB, offs))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB, hoffs))
+    d2h = hout.numel() * hout.element_size()
+    dA, dsA, dB, dsB, doffs = (torch.empty_like(t) for t in (A, sA, B, sB, offs))
+
+    def e2e_step():
+        for d, h in ((dA, hA), (dsA, hsA), (dB, hB), (dsB, hsB), (doffs, hoffs)):
+            d.copy_(h, non_blocking=True)
+        mx.wgrad_grouped(dA, dsA, dB, dsB, doffs, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    clocks = sampler.stop()
+
+    flop = float(w.flop)
+    ms_per_step = total_ms / K
+    value = world * flop / (ms_per_step * 1e-3) / 1e12
+    peak, peak_src, _ = mxfp8_peak()
+    main_avg = float(np.mean(main_ms))
+    achieved = flop / (main_avg * 1e-3) / 1e12
+    traffic = measured_traffic(args.config)
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            threads = len(os.sched_getaffinity(0))
+            rate, secs, desc = cpu_oracle_rate(A.cpu().numpy(), sA.cpu().numpy(), B.cpu().numpy(),
+                                               sB.cpu().numpy(), offs.cpu().numpy(), w, args.cpu_seconds, threads)
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{desc}; {secs:.1f} s on the host (fp64 plain loops)"}
+        result = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "mxfp8_e4m3 (e8m0 block-32 scales), fp32 accumulate, bf16 out",
+            "data": "synthetic (seeded routing and N(0,1)/Student-t operands, quantised on the GPU)",
+            "config": {"workload": args.config, "E": w.E, "N": w.N, "K": w.K, "M": w.M,
+                       "routing": w.description, "l2": "flushed (256 MiB write) before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_mxfp8_peak": 100.0 * value / world / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "wgrad_main", "peak_source": peak_src,
+                         "algorithmic_flop_per_launch": flop, "avg_launch_ms": main_avg},
+            "cpu_baseline": cpu,
+            "e2e": {"value": flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+        }
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+
+def _host_inputs(name: str):
+    """Host operands for the reference arm: seeded fp32 quantised by the
+    oracle's CPU quantiser (no GPU involved)."""
+    import oracle
+
+    w = I.WORKLOADS[name]
+    ops = []
+    for stream, rows in ((0, w.N), (1, w.K)):
+        q = np.empty((rows, w.M), np.uint8)
+        s = np.empty((rows, w.M // 32), np.uint8)
+        for r0 in range(0, rows, 256):
+            r1 = min(rows, r0 + 256)
+            q[r0:r1], s[r0:r1] = oracle.quantize_tokenwise(I.host_operand(r1 - r0, w.M, w.seed, stream, w.dist, row0=r0))
+        ops += [q, s]
+    return ops[0], ops[1], ops[2], ops[3], I.offsets(I.group_sizes(name))
+
+
+def bench_reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    w = I.WORKLOADS[args.config]
+    A, sA, B, sB, offs = _host_inputs(args.config)
+    threads = len(os.sched_getaffinity(0))
+    per_step = max(0.5, args.ref_step_seconds)
+    for i in range(args.warmup):
+        cpu_oracle_rate(A, sA, B, sB, offs, w, per_step / 4, threads, seed=i)
+    rates, secs, desc = [], 0.0, ""
+    for i in range(args.steps):
+        r, dt, desc = cpu_oracle_rate(A, sA, B, sB, offs, w, per_step, threads, seed=1000 + i)
+        rates.append(r)
+        secs += dt
+    value = float(np.mean(rates))
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (exact E4M3/E8M0 decode, fp64 accumulate, bf16 out)",
+        "data": "synthetic (seeded routing and N(0,1)/Student-t operands, quantised on the host)",
+        "config": {"workload": args.config, "E": w.E, "N": w.N, "K": w.K, "M": w.M, "routing": w.description},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {desc}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = bench_reference_arm(args) if args.impl == "reference" else bench_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -153,8 +153,8 @@ def test_tiny_workload_full():
 ])
 def test_edge_shapes(E, N, K, M, sizes):
     rng = np.random.default_rng(E * 1000 + N + K + M)
-    A, sA = rand_operand(rng, N, M)
-    B, sB = rand_operand(rng, K, M)
+    A, sA = quantised_operand(N, M, seed=E * 1000 + N, stream=0)
+    B, sB = quantised_operand(K, M, seed=E * 1000 + N, stream=1)
     if sizes is None:
         sizes = I.random_sizes(E, M, rng)
     offs = np.cumsum(sizes).astype(np.int32)
@@ -163,15 +163,44 @@ def test_edge_shapes(E, N, K, M, sizes):
 
 
 def test_varied_scales_move_rows_and_columns():
-    """Scales that vary per (row, 32-token block) on both operands: a misplaced
-    scale would shift whole rows or columns, far outside the tolerance."""
+    """Operands whose magnitude varies per row over 2^-6..2^6 before
+    quantisation, so scales vary per (row, 32-token block) on both operands: a
+    misplaced scale would shift whole rows or columns, far outside the
+    tolerance."""
     rng = np.random.default_rng(31)
     E, N, K, M = 2, 256, 512, 1024
-    A, sA = rand_operand(rng, N, M, 110, 145)
-    B, sB = rand_operand(rng, K, M, 110, 145)
+    xa = I.host_operand(N, M, seed=31, stream=0) * np.exp2(rng.integers(-6, 7, (N, 1))).astype(np.float32)
+    xb = I.host_operand(K, M, seed=31, stream=1) * np.exp2(rng.integers(-6, 7, (K, 1))).astype(np.float32)
+    A, sA = oracle.quantize_tokenwise(xa)
+    B, sB = oracle.quantize_tokenwise(xb)
+    assert len(np.unique(sA)) > 10 and len(np.unique(sB)) > 10
     offs = np.array([480, 1024], np.int32)
     got = run_gpu(A, sA, B, sB, offs, E, N, K)
     check_tol(got, A, sA, B, sB, offs, E, N, K, M)
+
+
+def test_extreme_dynamic_range():
+    """Uniformly random E4M3 codes (all magnitudes, subnormals included) with
+    independent scales over 2^-9..2^8 per 32-token block: sums cancel by up to
+    five orders of magnitude, so the bound is the one fp32 accumulation itself
+    gives. The tensor core adds each k = 32 block product into the fp32
+    accumulator; with L tokens that is at most L/32 + 32 roundings of a partial
+    sum bounded by sum|ab|, each at most 2^-24 of it, plus the final bf16
+    rounding (at most one bf16 ulp apart from the oracle's exact rounding):
+        |gpu - oracle| <= 2^-7 |oracle| + (L/32 + 32) 2^-24 sum|ab|."""
+    rng = np.random.default_rng(32)
+    E, N, K, M = 4, 384, 768, 2048
+    A, sA = rand_operand(rng, N, M)
+    B, sB = rand_operand(rng, K, M)
+    sizes = np.array([800, 352, 0, 896])
+    offs = np.cumsum(sizes).astype(np.int32)
+    got = run_gpu(A, sA, B, sB, offs, E, N, K)
+    ref, acc, aacc = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
+    L = sizes[:, None, None].astype(np.float64)
+    bound = 2.0 ** -7 * np.abs(oracle.bf16_bits_to_f64(ref)) + (L / 32 + 32) * 2.0 ** -24 * aacc
+    err = np.abs(oracle.bf16_bits_to_f64(got) - oracle.bf16_bits_to_f64(ref))
+    assert np.all(err <= bound)
+    assert np.all(got[2] == 0)
 
 
 # ------------------------------------------------------------------ properties
@@ -191,10 +220,9 @@ def test_bit_reproducible_and_workspace_variant():
 def test_padding_garbage_never_read():
     """NaN data and NaN scales past the last group give the same bits as the
     same call on operands cut down to their real token width."""
-    rng = np.random.default_rng(51)
     E, N, K, M = 3, 256, 512, 2048
-    A, sA = rand_operand(rng, N, M)
-    B, sB = rand_operand(rng, K, M)
+    A, sA = quantised_operand(N, M, seed=51, stream=0)
+    B, sB = quantised_operand(K, M, seed=51, stream=1)
     offs = np.array([416, 416, 1376], np.int32)
     Mc = int(offs[-1])
     cut = run_gpu(A[:, :Mc].copy(), sA[:, :Mc // 32].copy(), B[:, :Mc].copy(), sB[:, :Mc // 32].copy(),
@@ -208,10 +236,9 @@ def test_padding_garbage_never_read():
 
 
 def test_invalid_offsets_are_clamped_and_flagged():
-    rng = np.random.default_rng(61)
     E, N, K, M = 4, 128, 256, 1024
-    A, sA = rand_operand(rng, N, M)
-    B, sB = rand_operand(rng, K, M)
+    A, sA = quantised_operand(N, M, seed=61, stream=0)
+    B, sB = quantised_operand(K, M, seed=61, stream=1)
     mx.device_status(clear=True)
     bad = np.array([300, 200, 5000, 1024], np.int32)  # unaligned, decreasing, beyond M
     got = run_gpu(A, sA, B, sB, bad, E, N, K)
