@@ -134,6 +134,39 @@ const char* mxfp8_last_error(void);
  * `clear` is non-zero, resets it. Synchronises the current device first. */
 int mxfp8_device_status(int32_t* status, int clear);
 
+/* Capacity of the allocation-free entry point's scratch array (32 MiB). */
+#define MXFP8_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * Allocation-free variant of mxfp8_wgrad_grouped. The paper has no
+ * counterpart: this is an interface for callers that must not allocate. Some callers
+ * cannot call cudaMalloc and have no workspace to pass: a framework whose own
+ * caching allocator owns the device heap and forbids allocations behind its
+ * back, or a process that reserves its device memory up front and may not
+ * allocate afterwards. This entry point allocates nothing: it calls no
+ * cudaMalloc, cudaFree or allocating library routine. Its scratch (schedule
+ * and re-laid-out scale factors) lives in one fixed file-scope device array of
+ * MXFP8_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds
+ * until the process exits.
+ *
+ * Arguments, layouts, preconditions and results are those of
+ * mxfp8_wgrad_grouped; the caller still provides A, sA, B, sB, offs and out.
+ * Sizes whose scratch (mxfp8_wgrad_workspace_bytes) exceeds
+ * MXFP8_NOALLOC_SCRATCH_BYTES are rejected with MXFP8_ENOWS and a message,
+ * before any work is enqueued (e.g. the 16B shapes fit; the 671B shapes do not).
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture. Every call on a device shares the one
+ * array, and the array keeps whatever the last call left in it (each call
+ * rewrites all the scratch it reads, so nothing needs clearing): calls whose
+ * work overlaps on the GPU (different streams, no ordering between them) race
+ * on it and must be avoided by the caller.
+ */
+int mxfp8_wgrad_grouped_noalloc(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                                const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
+                                void* stream);
+
 /* Measurement hook: when both events are non-NULL, the next
  * mxfp8_wgrad_grouped{,_ws} call on this thread records `ev_before` on its
  * stream right before the main contraction kernel and `ev_after` right after

@@ -205,6 +205,8 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
 
 }  // namespace
 
+int mxw::set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 int mxfp8_wgrad_grouped(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,

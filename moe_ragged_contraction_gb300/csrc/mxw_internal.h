@@ -52,6 +52,9 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap& mapA, const CUte
 
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream);
 
+// Sets the calling thread's mxfp8_last_error() message; returns `code`.
+int set_last_error(int code, const char* msg);
+
 // Device status word (MXFP8_DEV_* bits).
 cudaError_t read_device_status(int32_t* status, int clear);
 

@@ -1,0 +1,89 @@
+"""The allocation-free entry point (mxfp8_wgrad_grouped_noalloc), called
+through the C ABI: its output matches the regular entry point's within the
+parity tolerance on two calls in a row, it allocates no device memory, and it
+rejects sizes whose scratch exceeds its fixed array. It exists for callers
+that cannot call cudaMalloc themselves (a framework whose allocator owns the
+device heap, or a process that reserved its memory up front).
+
+This file is collected last on purpose, and must pass both on its own in a
+fresh process and after the other tests."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_ragged_contraction_gb300 as mx
+from moe_ragged_contraction_gb300 import inputs as I
+
+from _util import quantised_operand, tolerance_violations
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mx.build()
+    lib = mx.load()
+    P, Ii, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.mxfp8_wgrad_grouped_noalloc.argtypes = [P, P, P, P, P, Ii, Ii, Ii, L, P, P]
+    lib.mxfp8_wgrad_grouped_noalloc.restype = Ii
+    return lib
+
+
+def free_bytes():
+    torch.cuda.synchronize()
+    return torch.cuda.mem_get_info()[0]
+
+
+@pytest.mark.parametrize("E,N,K,M,sizes", [
+    (4, 128, 256, 1024, "tiny"),
+    (6, 384, 768, 3072, [416, 0, 1024, 96, 1056, 480]),
+])
+def test_noalloc_matches_regular_entry_point(lib, E, N, K, M, sizes):
+    if sizes == "tiny":
+        sizes = I.group_sizes("tiny")
+    A, sA = quantised_operand(N, M, seed=900 + E, stream=0)
+    B, sB = quantised_operand(K, M, seed=900 + E, stream=1)
+    offs = np.cumsum(sizes).astype(np.int32)
+    d = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (A, sA, B, sB, offs)]
+    ptr = [ctypes.c_void_p(t.data_ptr()) for t in d]
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    ref = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    rc = lib.mxfp8_wgrad_grouped(*ptr, E, N, K, M, ctypes.c_void_p(ref.data_ptr()), stream)
+    assert rc == 0, lib.mxfp8_last_error()
+    ref_bits = ref.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    outs = [torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for o in outs:
+        o.view(torch.int16).fill_(-1)  # NaN-poison: unwritten elements would show
+    # warm call: the first call on a device resolves the scratch array's address
+    rc = lib.mxfp8_wgrad_grouped_noalloc(*ptr, E, N, K, M, ctypes.c_void_p(outs[0].data_ptr()), stream)
+    assert rc == 0, lib.mxfp8_last_error()
+    outs[0].view(torch.int16).fill_(-1)
+    before = free_bytes()
+    for o in outs:  # two calls in a row
+        rc = lib.mxfp8_wgrad_grouped_noalloc(*ptr, E, N, K, M, ctypes.c_void_p(o.data_ptr()), stream)
+        assert rc == 0, lib.mxfp8_last_error()
+    after = free_bytes()
+    assert after == before, f"device free memory changed by {before - after} bytes"
+
+    _, _, aacc = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
+    for o in outs:
+        got = o.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert not tolerance_violations(got, ref_bits, aacc).any()
+        assert np.array_equal(got, ref_bits)  # same kernels, same schedule: identical bits
+
+
+def test_noalloc_rejects_oversized(lib):
+    w = I.WORKLOADS["671Bgu"]
+    need = lib.mxfp8_wgrad_workspace_bytes(w.E, w.N, w.K, w.M)
+    assert need > (32 << 20)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: the size check comes first
+    rc = lib.mxfp8_wgrad_grouped_noalloc(fake, fake, fake, fake, fake, w.E, w.N, w.K, w.M, fake, None)
+    assert rc == -5
+    assert b"scratch" in lib.mxfp8_last_error()
