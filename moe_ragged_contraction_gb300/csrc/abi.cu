@@ -92,6 +92,23 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int rows, int64_t M,
     return MXFP8_OK;
 }
 
+// Scale-factor workspace viewed as u32 [blocks][128] (one 512-byte block per
+// row); boxes of box_blocks whole blocks, no swizzle.
+int make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t blocks, int box_blocks) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encoder(&enc);
+    if (rc) return rc;
+    cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(blocks)};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_blocks)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MXFP8_ECUDA, "cuTensorMapEncodeTiled (scales) failed (CUresult %d)", static_cast<int>(r));
+    return MXFP8_OK;
+}
+
 // Scratch cache keyed by (device, stream). Growth frees the old block in
 // stream order and allocates the new one in stream order, so earlier calls
 // on the same stream finish with the old block first.
@@ -180,10 +197,14 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
         rc = cached_workspace(dev, st, lay.total, &ws);
         if (rc) return rc;
     }
-    CUtensorMap mapA, mapB;
-    rc = make_operand_map(&mapA, A, N, M, mxw::BM);
+    CUtensorMap maps[4];
+    rc = make_operand_map(&maps[0], A, N, M, mxw::HALF_TILE_ROWS);
     if (rc) return rc;
-    rc = make_operand_map(&mapB, B, K, M, mxw::BN);
+    rc = make_operand_map(&maps[1], B, K, M, mxw::HALF_TILE_ROWS);
+    if (rc) return rc;
+    rc = make_sf_map(&maps[2], static_cast<uint8_t*>(ws) + lay.sfa_off, static_cast<int64_t>(lay.ntn) * lay.ts_max, 1);
+    if (rc) return rc;
+    rc = make_sf_map(&maps[3], static_cast<uint8_t*>(ws) + lay.sfb_off, static_cast<int64_t>(lay.ntk) * lay.ts_max * 2, 2);
     if (rc) return rc;
 
     mxw::WgradArgs a;
@@ -198,7 +219,7 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     a.ev_before = evb;
     a.ev_after = eva;
     const char* what = "";
-    cudaError_t e = mxw::launch_wgrad(a, mapA, mapB, &what);
+    cudaError_t e = mxw::launch_wgrad(a, maps, &what);
     if (e != cudaSuccess) return fail_cuda(e, what);
     return MXFP8_OK;
 }

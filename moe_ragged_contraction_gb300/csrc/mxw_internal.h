@@ -46,9 +46,15 @@ struct WgradArgs {
     cudaEvent_t ev_before, ev_after;
 };
 
+// Rows of A and of B that one CTA loads per K-step (the CTA's half of a
+// 256 x 256 pair tile).
+constexpr int HALF_TILE_ROWS = 128;
+
 // Enqueue the plan / scale re-layout kernel and the main contraction kernel.
-// Returns a cudaError_t; `what` names the failing step.
-cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB, const char** what);
+// maps: A and B operand tiles (HALF_TILE_ROWS rows x BK tokens, 128-byte
+// swizzle) and the scale-factor workspaces viewed as u32 [blocks][128]
+// (boxes of 1 and 2 blocks). Returns a cudaError_t; `what` names the step.
+cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what);
 
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream);
 

@@ -40,18 +40,28 @@ __device__ int g_device_status = 0;
 // ============================================================== prep kernel
 
 constexpr int PREP_THREADS = 256;
-constexpr int PREP_WARPS = PREP_THREADS / 32;
+constexpr int PREP_ROWS = 128;                           // rows of one scale-factor block
+constexpr int PREP_TASKS_PER_CTA = PREP_THREADS / PREP_ROWS;
+constexpr int PREP_STEPS_PER_TASK = 4;                   // K-steps gathered by one thread per task
 
-// grid: x = ceil(ts_max / PREP_WARPS) groups of K-steps, y = ntn + 2 * ntk
-// 128-row blocks (A blocks first, then B blocks). Each warp writes one
-// 512-byte scale-factor block: lane r0 writes bytes [16 r0, 16 r0 + 16),
-// holding rows r0 + 32 j (j = 0..3) x 4 consecutive 32-token blocks.
+// Every block first rebuilds the per-expert runs from offs (one warp, shuffle
+// scans; E <= MXFP8_MAX_EXPERTS words of shared memory). Block 0 also writes
+// the plan. Then the blocks stride over tasks (128-row block rb, group of 4
+// global K-steps): thread r of a task owns row r and gathers its 4 scale
+// bytes for each of the 4 K-steps (16 independent loads), writing them into
+// the 512-byte scale-factor blocks, where row r, 32-token block kb sits at
+// byte (r % 32) * 16 + (r / 32) * 4 + kb. Row blocks: A's ceil(N/128) first,
+// then B's, two per 256-row B tile.
 __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs,
                                                            const uint8_t* __restrict__ sA,
                                                            const uint8_t* __restrict__ sB,
                                                            int32_t* __restrict__ plan, uint8_t* __restrict__ sfa,
                                                            uint8_t* __restrict__ sfb, int E, int N, int K,
                                                            long long M, int ts_max, int ntn, int ntk) {
+    // the main kernel may start its prologue now; it waits for this grid's
+    // completion before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     extern __shared__ int prep_smem[];
     int* s_start = prep_smem;        // [E]
     int* s_end = s_start + E;        // [E]
@@ -108,7 +118,7 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     __syncthreads();
     const int TS = s_sb[E];
 
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
+    if (blockIdx.x == 0) {
         if (threadIdx.x == 0) {
             plan[0] = TS;
             plan[1] = E;
@@ -131,57 +141,76 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         }
     }
 
-    const int gs = blockIdx.x * PREP_WARPS + warp;  // global K-step of this warp
-    if (gs >= TS) return;
-    // expert owning global K-step gs: the last g with s_sb[g] <= gs
-    int lo = 0, hi = E;  // invariant: s_sb[lo] <= gs < s_sb[hi] (s_sb[E] = TS)
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_sb[mid] <= gs) lo = mid; else hi = mid;
-    }
-    const int g = lo;
-    const long long t0 = static_cast<long long>(s_start[g]) + static_cast<long long>(gs - s_sb[g]) * BK;
-    const long long tend = s_end[g];
-
-    const int rb = blockIdx.y;
-    const uint8_t* plane;
-    int rows, row0;
-    uint8_t* dst;
-    if (rb < ntn) {
-        plane = sA; rows = N; row0 = rb * BM;
-        dst = sfa + (static_cast<size_t>(rb) * ts_max + gs) * SF_ATOM;
-    } else {
-        const int rbb = rb - ntn;
-        plane = sB; rows = K; row0 = rbb * BM;
-        dst = sfb + ((static_cast<size_t>(rbb >> 1) * ts_max + gs) * 2 + (rbb & 1)) * SF_ATOM;
-    }
+    const int ngq = (TS + PREP_STEPS_PER_TASK - 1) / PREP_STEPS_PER_TASK;
+    const long long ntasks = static_cast<long long>(ntn + 2 * ntk) * ngq;
+    const int r = threadIdx.x % PREP_ROWS;
     const long long sM = M / 32;
-    uint32_t w[4];
+    for (long long task = static_cast<long long>(blockIdx.x) * PREP_TASKS_PER_CTA + threadIdx.x / PREP_ROWS;
+         task < ntasks; task += static_cast<long long>(gridDim.x) * PREP_TASKS_PER_CTA) {
+        const int rb = static_cast<int>(task / ngq);
+        const int gq = static_cast<int>(task - static_cast<long long>(rb) * ngq);
+        const uint8_t* plane;
+        int rows, row;
+        uint8_t* dst;       // scale-factor block of global K-step 0 for this row block
+        size_t dst_step;    // bytes between consecutive global K-steps
+        if (rb < ntn) {
+            plane = sA; rows = N; row = rb * BM + r;
+            dst = sfa + static_cast<size_t>(rb) * ts_max * SF_ATOM;
+            dst_step = SF_ATOM;
+        } else {
+            const int rbb = rb - ntn;
+            plane = sB; rows = K; row = rbb * BM + r;
+            dst = sfb + (static_cast<size_t>(rbb >> 1) * ts_max * 2 + (rbb & 1)) * SF_ATOM;
+            dst_step = 2 * SF_ATOM;
+        }
+        const uint8_t* src = plane + static_cast<size_t>(row) * sM;
+        uint32_t w[PREP_STEPS_PER_TASK];
+        int gsv[PREP_STEPS_PER_TASK];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int row = row0 + lane + 32 * j;
-        uint32_t word = 0;
+        for (int j = 0; j < PREP_STEPS_PER_TASK; ++j) {
+            const int gs = gq * PREP_STEPS_PER_TASK + j;
+            gsv[j] = gs;
+            w[j] = 0;
+            if (gs < TS) {
+                int lo = 0, hi = E;  // expert owning gs: the last g with s_sb[g] <= gs
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_sb[mid] <= gs) lo = mid; else hi = mid;
+                }
+                const long long t0 = static_cast<long long>(s_start[lo]) + static_cast<long long>(gs - s_sb[lo]) * BK;
+                const long long tend = s_end[lo];
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-            const long long t = t0 + 32 * kb;
-            if (row < rows && t < tend) {
-                const uint32_t b = __ldg(plane + static_cast<size_t>(row) * sM + (t >> 5));
-                word |= b << (8 * kb);
+                for (int kb = 0; kb < 4; ++kb) {
+                    const long long t = t0 + 32 * kb;
+                    if (row < rows && t < tend) w[j] |= static_cast<uint32_t>(__ldg(src + (t >> 5))) << (8 * kb);
+                }
             }
         }
-        w[j] = word;
+        const int off = (r & 31) * 16 + (r >> 5) * 4;
+#pragma unroll
+        for (int j = 0; j < PREP_STEPS_PER_TASK; ++j)
+            if (gsv[j] < TS) *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(gsv[j]) * dst_step + off) = w[j];
     }
-    reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ============================================================== main kernel
 
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK;   // 16 KB
-constexpr int B_STAGE = BN * BK;   // 32 KB
-constexpr int SFA_STAGE = SF_ATOM;
-constexpr int SFB_STAGE = 2 * SF_ATOM;
-constexpr uint32_t TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+// One CTA pair (a 2-CTA cluster) owns a 256 x 256 output tile: rows
+// [nt*256, nt*256+256) of A (the N axis) by rows [kt*256, kt*256+256) of B
+// (the K axis). CTA r of the pair holds A rows nt*256 + 128r .. +128 and B
+// rows kt*256 + 128r .. +128 in its shared memory, its own 128 accumulator
+// rows in its TMEM, and stores those 128 output rows. The leader (r = 0)
+// issues the M = 256 block-scaled MMAs for both; each SM then reads 32 KB of
+// operands per K-step instead of the 48 KB a 128 x 256 single-CTA tile needs.
+constexpr int PAIR_M = 2 * BM;    // 256 rows of A per pair tile
+constexpr int HALF_N = BN / 2;    // 128 rows of B per CTA
+constexpr int STAGES = 6;
+constexpr int A_STAGE = BM * BK;       // 16 KB
+constexpr int B_STAGE = HALF_N * BK;   // 16 KB
+constexpr int SFA_STAGE = SF_ATOM;     // this CTA's 128 A rows
+constexpr int SFB_STAGE = 2 * SF_ATOM; // all 256 B rows of the tile (each CTA's MMA half needs them)
+constexpr uint32_t CTA_TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+constexpr uint32_t PAIR_TX_BYTES = 2 * CTA_TX_BYTES;
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
@@ -192,39 +221,49 @@ constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int MAIN_SMEM = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 constexpr int EPI_WARPS = 8;
-constexpr int MAIN_THREADS = 32 * (2 + EPI_WARPS);
+constexpr int MAIN_THREADS = 32 * (3 + EPI_WARPS);  // producer, MMA issuer, stage watcher, epilogue
+// Named barriers between the stage watcher and the MMA warp (64 threads each):
+// BAR_READY + st: stage st holds data (watcher arrives, MMA warp syncs);
+// BAR_FREE + st: the MMA warp has taken stage st (MMA warp arrives, watcher
+// syncs before it signals that stage again), so arrivals and syncs on every
+// id pair up one to one.
+constexpr uint32_t BAR_READY = 1;
+constexpr uint32_t BAR_FREE = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SFA = 256;  // + 4 * stage: 4 columns of A scales per stage
 constexpr uint32_t TMEM_SFB = 288;  // + 8 * stage: 8 columns of B scales per stage
 
 static_assert(OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(TMEM_SFB + 8 * STAGES <= TMEM_COLS, "TMEM budget");
+static_assert(TMEM_SFA + 4 * STAGES <= TMEM_SFB && TMEM_SFB + 8 * STAGES <= TMEM_COLS, "TMEM budget");
+static_assert(MAIN_SMEM <= 232448, "shared memory budget");
+static_assert(BAR_READY + STAGES <= BAR_FREE && BAR_FREE + STAGES <= 16, "named barrier ids");
 
 // Instruction descriptor, kind::mxf8f6f4: A and B E4M3 (0), both K-major,
-// N >> 3 at bits 17-22, E8M0 scales (bit 23), M >> 4 at bits 24-28; the scale
-// byte selectors for B (bits 4-5) and A (bits 29-30) are or-ed in per MMA.
+// N >> 3 at bits 17-22, E8M0 scales (bit 23), M >> 4 at bits 24-28 (M = 256
+// across the pair); the scale byte selectors for B (bits 4-5) and A (bits
+// 29-30) are or-ed in per MMA.
 constexpr uint32_t IDESC_BASE = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-                                (static_cast<uint32_t>(BM >> 4) << 24);
+                                (static_cast<uint32_t>(PAIR_M >> 4) << 24);
 
 struct MainParams {
     const int32_t* plan;
-    const uint8_t* sfa;
-    const uint8_t* sfb;
     uint16_t* out;
     int E, N, K;
-    int ts_max, ntn, ntk;
+    int ts_max, ntn2, ntk;   // ntn2 = ceil(N / 256) pair-tile rows
     unsigned long long wait_ns;
 };
 
 // Bounded wait: returns false (and raises the CTA's abort flag and the device
 // status word) if the phase does not complete within wait_ns, or returns
-// false at once if another role already aborted.
+// false at once if another role of this CTA already aborted.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned long long wait_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto done = [&] { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (done()) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (done()) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > wait_ns) {
             *abort_flag = 1;
@@ -234,7 +273,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
-// Bounded wait used while tearing down after an abort (ignores the flag).
+// Bounded wait used while tearing down (ignores the abort flag).
 __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, unsigned long long wait_ns) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
@@ -249,8 +288,8 @@ struct Item {
     int g, nt, kt, start, len, nsteps, step_base;
 };
 
-// Work item i (in longest-expert-first order, tiles of one expert
-// consecutive, K-tiles fastest) -> expert and tile.
+// Work item i (in longest-expert-first order, the tiles of one expert
+// consecutive, K-tiles fastest) -> expert and pair tile.
 __device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int E, int ntk, int nt_per_expert,
                                           long long i) {
     const int32_t* ex = plan + PLAN_HDR;
@@ -268,19 +307,24 @@ __device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int 
     return it;
 }
 
-// Static schedule: pass p hands items [p*G, (p+1)*G) to the CTAs, reversing
-// the direction on odd passes so that, with items sorted by cost, the loads
-// even out (no atomics; every CTA knows its items from its index alone).
-__device__ __forceinline__ long long item_index(long long pass, int G, int cta) {
-    return pass * G + ((pass & 1) ? (G - 1 - cta) : cta);
+// Static schedule over CTA pairs: pass p hands items [p*G, (p+1)*G) to the
+// pairs, reversing the direction on odd passes so that, with items sorted by
+// cost, the loads even out (no atomics; a pair knows its items from its
+// index alone, and both CTAs of a pair walk the same list).
+__device__ __forceinline__ long long item_index(long long pass, int G, int pair) {
+    return pass * G + ((pass & 1) ? (G - 1 - pair) : pair);
 }
 
-__global__ void __launch_bounds__(MAIN_THREADS, 1)
-    wgrad_main(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const MainParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
+    wgrad_main(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+               const MainParams p) {
     extern __shared__ uint8_t main_smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(main_smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
+    const bool leader = rank == 0;
 
     const uint32_t bar_full = sbase + OFF_BAR;
     const uint32_t bar_empty = bar_full + 8 * STAGES;
@@ -292,57 +336,63 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, 1);    // leader's arrive.expect_tx for both CTAs' bytes
+            mbar_init(bar_empty + 8 * s, 1);   // leader's MMA commit, multicast to both CTAs
         }
-        mbar_init(bar_tfull, 1);
-        mbar_init(bar_tempty, EPI_WARPS);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_tfull, 1);               // leader's commit after a tile, multicast
+        mbar_init(bar_tempty, 2 * EPI_WARPS);  // epilogue warps of both CTAs (leader's copy is used)
+        mbar_init(bar_drain, 1);               // leader's final commit, multicast
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSFA);
+        tma_prefetch_desc(&tmSFB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // everything below reads the plan and scale blocks of the preceding kernel
+    griddep_wait();
 
-    const int nt_per_expert = p.ntn * p.ntk;
+    const int nt_per_expert = p.ntn2 * p.ntk;
     const long long total = static_cast<long long>(p.E) * nt_per_expert;
-    const int G = gridDim.x, cta = blockIdx.x;
+    const int G = gridDim.x / 2, pair = blockIdx.x / 2;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
+            const uint32_t full_leader = mapa_shared(bar_full, 0);
             uint32_t c = 0;
             bool ok = true;
             for (long long pass = 0; ok && pass * G < total; ++pass) {
-                const long long i = item_index(pass, G, cta);
+                const long long i = item_index(pass, G, pair);
                 if (i >= total) continue;
                 const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
+                const int a_row = it.nt * PAIR_M + static_cast<int>(rank) * BM;
+                const int b_row = it.kt * BN + static_cast<int>(rank) * HALF_N;
+                const int sfa_row = (it.nt * 2 + static_cast<int>(rank)) * p.ts_max + it.step_base;
+                const int sfb_row = (it.kt * p.ts_max + it.step_base) * 2;
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
                     const int st = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
                     if (!wait_phase(bar_empty + 8 * st, ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
-                    const uint32_t fb = bar_full + 8 * st;
-                    mbar_arrive_expect_tx(fb, TX_BYTES);
+                    const uint32_t fb = full_leader + 8 * st;
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * st, PAIR_TX_BYTES);
                     const int x = it.start + s * BK;
-                    tma_load_2d(sbase + OFF_A + st * A_STAGE, &tmA, fb, x, it.nt * BM);
-                    tma_load_2d(sbase + OFF_B + st * B_STAGE, &tmB, fb, x, it.kt * BN);
-                    const size_t gstep = static_cast<size_t>(it.step_base + s);
-                    bulk_g2s(sbase + OFF_SFA + st * SFA_STAGE,
-                             p.sfa + (static_cast<size_t>(it.nt) * p.ts_max + gstep) * SF_ATOM, SFA_STAGE, fb);
-                    bulk_g2s(sbase + OFF_SFB + st * SFB_STAGE,
-                             p.sfb + (static_cast<size_t>(it.kt) * p.ts_max + gstep) * (2 * SF_ATOM), SFB_STAGE, fb);
+                    tma_load_2d_pair(sbase + OFF_A + st * A_STAGE, &tmA, fb, x, a_row);
+                    tma_load_2d_pair(sbase + OFF_B + st * B_STAGE, &tmB, fb, x, b_row);
+                    tma_load_2d_pair(sbase + OFF_SFA + st * SFA_STAGE, &tmSFA, fb, 0, sfa_row + s);
+                    tma_load_2d_pair(sbase + OFF_SFB + st * SFB_STAGE, &tmSFB, fb, 0, sfb_row + 2 * s);
                 }
             }
-            if (!ok || *abort_flag) {
-                // let every copy still in flight land before the CTA exits
+            if (leader && (!ok || *abort_flag)) {
+                // let every copy still in flight land before the pair exits
                 const uint32_t n = c < STAGES ? c : STAGES;
                 for (uint32_t d = 1; d <= n; ++d) {
                     const uint32_t j = c - d;
@@ -352,60 +402,103 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        // The whole warp walks the schedule; one elected lane issues each
+        // tcgen05 operation. The per-stage loop reads no memory: a load or an
+        // mbarrier probe here stalls this warp long enough to drain the
+        // tensor pipe, so stage readiness arrives through named barriers from
+        // the watcher warp. After an abort the loop still walks every stage
+        // (skipping the tensor work) so that the named barriers stay paired.
+        if (leader) {
             uint32_t c = 0, tiles = 0;
-            bool ok = true;
-            for (long long pass = 0; ok && pass * G < total; ++pass) {
-                const long long i = item_index(pass, G, cta);
+            bool live = true;
+            for (long long pass = 0; pass * G < total; ++pass) {
+                const long long i = item_index(pass, G, pair);
                 if (i >= total) continue;
                 const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
                 if (it.nsteps == 0) continue;
-                if (!wait_phase(bar_tempty, (tiles & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
+                if (live) {
+                    bool ok = true;
+                    // both CTAs' epilogues have drained the accumulator (peer arrivals are remote)
+                    if (lane == 0) ok = !*abort_flag && wait_phase<true>(bar_tempty, (tiles & 1) ^ 1, abort_flag, p.wait_ns);
+                    live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
                 tc_fence_after();
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
-                    const int st = c % STAGES;
-                    const uint32_t ph = (c / STAGES) & 1;
-                    if (!wait_phase(bar_full + 8 * st, ph, abort_flag, p.wait_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sfa_t = tmem + TMEM_SFA + 4 * st;
-                    const uint32_t sfb_t = tmem + TMEM_SFB + 8 * st;
-                    const uint32_t sfa_s = sbase + OFF_SFA + st * SFA_STAGE;
-                    const uint32_t sfb_s = sbase + OFF_SFB + st * SFB_STAGE;
-                    tc_cp_32x128b_warpx4(sfa_t, desc_sf_block(sfa_s));
-                    tc_cp_32x128b_warpx4(sfb_t, desc_sf_block(sfb_s));
-                    tc_cp_32x128b_warpx4(sfb_t + 4, desc_sf_block(sfb_s + SF_ATOM));
-                    const int rem = it.len - s * BK;
-                    const int nk = rem >= BK ? 4 : (rem >> 5);
-                    const uint32_t a_s = sbase + OFF_A + st * A_STAGE;
-                    const uint32_t b_s = sbase + OFF_B + st * B_STAGE;
-                    for (int kk = 0; kk < nk; ++kk) {
-                        const uint32_t idesc = IDESC_BASE | (static_cast<uint32_t>(kk) << 29) |
-                                               (static_cast<uint32_t>(kk) << 4);
-                        tc_mma_mxf8(tmem, desc_kmajor_sw128(a_s + 32 * kk), desc_kmajor_sw128(b_s + 32 * kk), idesc,
-                                    sfa_t, sfb_t, (s > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t st = c % STAGES;
+                    named_bar_sync(BAR_READY + st, 64);
+                    if (live) {
+                        tc_fence_after();
+                        const uint32_t sfa_t = tmem + TMEM_SFA + 4 * st;
+                        const uint32_t sfb_t = tmem + TMEM_SFB + 8 * st;
+                        const uint32_t sfa_s = sbase + OFF_SFA + st * SFA_STAGE;
+                        const uint32_t sfb_s = sbase + OFF_SFB + st * SFB_STAGE;
+                        tc_cp_32x128b_warpx4_pair_elect(sfa_t, desc_sf_block(sfa_s));
+                        tc_cp_32x128b_warpx4_pair_elect(sfb_t, desc_sf_block(sfb_s));
+                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 4, desc_sf_block(sfb_s + SF_ATOM));
+                        const int rem = it.len - s * BK;
+                        const int nk = rem >= BK ? 4 : (rem >> 5);
+                        const uint32_t a_s = sbase + OFF_A + st * A_STAGE;
+                        const uint32_t b_s = sbase + OFF_B + st * B_STAGE;
+                        for (int kk = 0; kk < nk; ++kk) {
+                            const uint32_t idesc = IDESC_BASE | (static_cast<uint32_t>(kk) << 29) |
+                                                   (static_cast<uint32_t>(kk) << 4);
+                            tc_mma_mxf8_pair_elect(tmem, desc_kmajor_sw128(a_s + 32 * kk),
+                                                   desc_kmajor_sw128(b_s + 32 * kk), idesc, sfa_t, sfb_t,
+                                                   (s > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair_elect(bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
                     }
-                    tc_commit(bar_empty + 8 * st);  // frees the stage once these MMAs have read it
+                    named_bar_arrive(BAR_FREE + st, 64);
                 }
-                if (!ok) break;
-                tc_commit(bar_tfull);  // accumulator complete
-                ++tiles;
+                if (live) {
+                    tc_commit_pair_elect(bar_tfull, 0x3);  // both accumulator halves complete
+                    ++tiles;
+                }
             }
-            // every MMA / copy this thread issued has finished before teardown
-            tc_commit(bar_drain);
-            drain_phase(bar_drain, 0, p.wait_ns);
+            // every MMA / copy issued for the pair has finished before teardown
+            tc_commit_pair_elect(bar_drain, 0x3);
+        }
+        if (lane == 0) drain_phase(bar_drain, 0, p.wait_ns);
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ stage watcher (leader only)
+        // Waits (bounded) for each stage's data and hands it to the MMA warp
+        // through BAR_READY; after an abort it stops waiting but keeps the
+        // barrier pairing until the schedule ends.
+        if (leader) {
+            uint32_t c = 0;
+            bool live = true;
+            for (long long pass = 0; pass * G < total; ++pass) {
+                const long long i = item_index(pass, G, pair);
+                if (i >= total) continue;
+                const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
+                for (int s = 0; s < it.nsteps; ++s, ++c) {
+                    const uint32_t st = c % STAGES;
+                    if (c >= STAGES) named_bar_sync(BAR_FREE + st, 64);  // MMA warp took the previous fill
+                    if (live) {
+                        bool ok = true;
+                        if (lane == 0) ok = wait_phase(bar_full + 8 * st, (c / STAGES) & 1, abort_flag, p.wait_ns);
+                        live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    }
+                    named_bar_arrive(BAR_READY + st, 64);
+                }
+            }
+            // consume the MMA warp's last BAR_FREE arrivals so every id ends paired
+            for (uint32_t d = c < STAGES ? c : STAGES; d > 0; --d) named_bar_sync(BAR_FREE + (c - d) % STAGES, 64);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (8 warps)
+        // ------------------------------------------------ epilogue (8 warps per CTA)
         const int q = warp & 3;          // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;   // column half of the 256-wide tile
+        const int h = (warp - 3) >> 2;   // column half of the 256-wide tile
+        const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
         uint32_t tiles = 0;
         for (long long pass = 0; pass * G < total; ++pass) {
-            const long long i = item_index(pass, G, cta);
+            const long long i = item_index(pass, G, pair);
             if (i >= total) continue;
             const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
-            const int row = it.nt * BM + q * 32 + lane;
+            const int row = it.nt * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;
             const int col0 = it.kt * BN + h * 128;
             uint16_t* orow = p.out + (static_cast<size_t>(it.g) * p.N + row) * static_cast<size_t>(p.K) + col0;
             if (it.nsteps == 0) {
@@ -416,7 +509,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
                 }
                 continue;
             }
-            if (!wait_phase(bar_tfull, tiles & 1, abort_flag, p.wait_ns)) break;
+            // one lane waits, the warp follows its verdict (the TMEM loads below
+            // are warp-collective, so the lanes must not split on a timeout)
+            bool ready = true;
+            if (lane == 0) ready = wait_phase(bar_tfull, tiles & 1, abort_flag, p.wait_ns);
+            if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
             tc_fence_after();
             uint32_t v[4][32];
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 128);
@@ -427,7 +524,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
             for (int j = 0; j < 4; ++j) reg_fence(v[j]);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty);  // accumulator may be overwritten
+            if (lane == 0) {
+                // this CTA's accumulator half may be overwritten
+                if (leader) mbar_arrive(bar_tempty);
+                else mbar_arrive_cluster(tempty_leader);
+            }
             ++tiles;
             if (row < p.N) {
 #pragma unroll
@@ -448,10 +549,12 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         }
     }
 
+    // both CTAs stay resident until the pair's MMAs, copies and TMEM reads are
+    // done, then free the pair's TMEM together
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
 // ============================================================== host side
@@ -472,7 +575,7 @@ bool ws_layout(int E, int N, int K, int64_t M, WsLayout* L) {
     return true;
 }
 
-cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB, const char** what) {
+cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what) {
     const WsLayout& L = a.lay;
     int32_t* plan = reinterpret_cast<int32_t*>(a.ws + L.plan_off);
     uint8_t* sfa = a.ws + L.sfa_off;
@@ -480,42 +583,69 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap& mapA, const CUte
 
     *what = "plan / scale re-layout kernel";
     {
-        dim3 grid((L.ts_max + PREP_WARPS - 1) / PREP_WARPS, L.ntn + 2 * L.ntk);
+        // enough blocks for every task of the largest possible plan, at most 6 per SM
+        const long long tasks = static_cast<long long>(L.ntn + 2 * L.ntk) *
+                                ((L.ts_max + PREP_STEPS_PER_TASK - 1) / PREP_STEPS_PER_TASK);
+        long long blocks = (tasks + PREP_TASKS_PER_CTA - 1) / PREP_TASKS_PER_CTA;
+        if (blocks > 6LL * a.num_sms) blocks = 6LL * a.num_sms;
+        if (blocks < 1) blocks = 1;
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1);
-        wgrad_prep<<<grid, PREP_THREADS, sm, a.stream>>>(a.offs, a.sA, a.sB, plan, sfa, sfb, a.E, a.N, a.K, a.M,
-                                                         L.ts_max, L.ntn, L.ntk);
+        wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(
+            a.offs, a.sA, a.sB, plan, sfa, sfb, a.E, a.N, a.K, a.M, L.ts_max, L.ntn, L.ntk);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
 
     *what = "main contraction kernel";
-    static bool attr_set[64] = {};  // the attribute is set once per device
+    // per device: the shared-memory opt-in and the number of CTA pairs that
+    // can be resident at once (the persistent grid)
+    static int max_pairs[64] = {};
     if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[a.dev]) {
+    if (max_pairs[a.dev] == 0) {
         cudaError_t e = cudaFuncSetAttribute(wgrad_main, cudaFuncAttributeMaxDynamicSharedMemorySize, MAIN_SMEM);
         if (e != cudaSuccess) return e;
-        attr_set[a.dev] = true;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * (a.num_sms / 2));
+        q.blockDim = dim3(MAIN_THREADS);
+        q.dynamicSmemBytes = MAIN_SMEM;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, wgrad_main, &q);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        max_pairs[a.dev] = clusters;
     }
     MainParams mp;
     mp.plan = plan;
-    mp.sfa = sfa;
-    mp.sfb = sfb;
     mp.out = a.out;
     mp.E = a.E;
     mp.N = a.N;
     mp.K = a.K;
     mp.ts_max = L.ts_max;
-    mp.ntn = L.ntn;
+    mp.ntn2 = (a.N + PAIR_M - 1) / PAIR_M;
     mp.ntk = L.ntk;
     mp.wait_ns = a.wait_limit_ns;
-    const long long total = static_cast<long long>(a.E) * L.ntn * L.ntk;
-    const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
+    const long long total = static_cast<long long>(a.E) * mp.ntn2 * mp.ntk;
+    const int pairs = static_cast<int>(total < max_pairs[a.dev] ? total : max_pairs[a.dev]);
     if (a.ev_before) {
         cudaError_t e = cudaEventRecord(a.ev_before, a.stream);
         if (e != cudaSuccess) return e;
     }
-    wgrad_main<<<grid, MAIN_THREADS, MAIN_SMEM, a.stream>>>(mapA, mapB, mp);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the prologue (barriers, TMEM allocation,
+    // descriptor prefetch) overlaps the prep kernel; griddepcontrol.wait in
+    // the kernel orders every read of the prep kernel's output after it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(MAIN_THREADS);
+    cfg.dynamicSmemBytes = MAIN_SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], mp);
+    if (e != cudaSuccess) return e;
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.ev_after) {
         e = cudaEventRecord(a.ev_after, a.stream);
