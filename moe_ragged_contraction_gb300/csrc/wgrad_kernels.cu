@@ -40,28 +40,21 @@ __device__ int g_device_status = 0;
 // ============================================================== prep kernel
 
 constexpr int PREP_THREADS = 256;
-constexpr int PREP_ROWS = 128;                           // rows of one scale-factor block
-constexpr int PREP_TASKS_PER_CTA = PREP_THREADS / PREP_ROWS;
-constexpr int PREP_STEPS_PER_TASK = 4;                   // K-steps gathered by one thread per task
+constexpr int PREP_ROWS = 128;        // rows of one scale-factor block
+constexpr int PREP_TILE_STEPS = 32;   // K-steps per gather task (one per lane)
 
 // Every block first rebuilds the per-expert runs from offs (one warp, shuffle
-// scans; E <= MXFP8_MAX_EXPERTS words of shared memory). Block 0 also writes
-// the plan. Then the blocks stride over tasks (128-row block rb, group of 4
-// global K-steps): thread r of a task owns row r and gathers its 4 scale
-// bytes for each of the 4 K-steps (16 independent loads), writing them into
-// the 512-byte scale-factor blocks, where row r, 32-token block kb sits at
-// byte (r % 32) * 16 + (r / 32) * 4 + kb. Row blocks: A's ceil(N/128) first,
-// then B's, two per 256-row B tile.
+// scans; 3E + 1 words of shared memory). Block 0 also writes the plan. Then
+// the blocks stride over gather tasks (below), writing the 512-byte
+// scale-factor blocks, where row r, 32-token block kb sits at byte
+// (r % 32) * 16 + (r / 32) * 4 + kb. Row blocks: A's ceil(N/128) first, then
+// B's, two per 256-row B tile.
 __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs,
                                                            const uint8_t* __restrict__ sA,
                                                            const uint8_t* __restrict__ sB,
                                                            int32_t* __restrict__ plan, uint8_t* __restrict__ sfa,
                                                            uint8_t* __restrict__ sfb, int E, int N, int K,
                                                            long long M, int ts_max, int ntn, int ntk) {
-    // the main kernel may start its prologue now; it waits for this grid's
-    // completion before it reads anything written here
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
     extern __shared__ int prep_smem[];
     int* s_start = prep_smem;        // [E]
     int* s_end = s_start + E;        // [E]
@@ -141,56 +134,77 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         }
     }
 
-    const int ngq = (TS + PREP_STEPS_PER_TASK - 1) / PREP_STEPS_PER_TASK;
-    const long long ntasks = static_cast<long long>(ntn + 2 * ntk) * ngq;
-    const int r = threadIdx.x % PREP_ROWS;
+    // Scale-factor gather as a tile transpose: a task is (128-row block rb,
+    // 32 consecutive global K-steps). Lane l of a warp owns K-step gs0 + l and
+    // loads that step's 4 scale bytes of one row, so consecutive lanes read
+    // consecutive 4-byte groups of the row (coalesced within an expert); the
+    // words are staged in a padded [128][33] shared tile, then each 512-byte
+    // block is written by one warp with 16-byte stores.
+    uint32_t* tile = reinterpret_cast<uint32_t*>(s_sb + E + 1);  // [PREP_ROWS][PREP_TILE_STEPS + 1]
+    const int nchunks = (TS + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS;
+    const long long ntasks = static_cast<long long>(ntn + 2 * ntk) * nchunks;
     const long long sM = M / 32;
-    for (long long task = static_cast<long long>(blockIdx.x) * PREP_TASKS_PER_CTA + threadIdx.x / PREP_ROWS;
-         task < ntasks; task += static_cast<long long>(gridDim.x) * PREP_TASKS_PER_CTA) {
-        const int rb = static_cast<int>(task / ngq);
-        const int gq = static_cast<int>(task - static_cast<long long>(rb) * ngq);
+    for (long long task = blockIdx.x; task < ntasks; task += gridDim.x) {
+        const int rb = static_cast<int>(task / nchunks);
+        const int gs0 = static_cast<int>(task - static_cast<long long>(rb) * nchunks) * PREP_TILE_STEPS;
         const uint8_t* plane;
-        int rows, row;
+        int rows, row0;
         uint8_t* dst;       // scale-factor block of global K-step 0 for this row block
         size_t dst_step;    // bytes between consecutive global K-steps
         if (rb < ntn) {
-            plane = sA; rows = N; row = rb * BM + r;
+            plane = sA; rows = N; row0 = rb * BM;
             dst = sfa + static_cast<size_t>(rb) * ts_max * SF_ATOM;
             dst_step = SF_ATOM;
         } else {
             const int rbb = rb - ntn;
-            plane = sB; rows = K; row = rbb * BM + r;
+            plane = sB; rows = K; row0 = rbb * BM;
             dst = sfb + (static_cast<size_t>(rbb >> 1) * ts_max * 2 + (rbb & 1)) * SF_ATOM;
             dst_step = 2 * SF_ATOM;
         }
-        const uint8_t* src = plane + static_cast<size_t>(row) * sM;
-        uint32_t w[PREP_STEPS_PER_TASK];
-        int gsv[PREP_STEPS_PER_TASK];
-#pragma unroll
-        for (int j = 0; j < PREP_STEPS_PER_TASK; ++j) {
-            const int gs = gq * PREP_STEPS_PER_TASK + j;
-            gsv[j] = gs;
-            w[j] = 0;
-            if (gs < TS) {
-                int lo = 0, hi = E;  // expert owning gs: the last g with s_sb[g] <= gs
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (s_sb[mid] <= gs) lo = mid; else hi = mid;
-                }
-                const long long t0 = static_cast<long long>(s_start[lo]) + static_cast<long long>(gs - s_sb[lo]) * BK;
-                const long long tend = s_end[lo];
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
-                    const long long t = t0 + 32 * kb;
-                    if (row < rows && t < tend) w[j] |= static_cast<uint32_t>(__ldg(src + (t >> 5))) << (8 * kb);
-                }
+        // this lane's K-step: its expert, first scale column and valid 32-token blocks
+        const int gs = gs0 + lane;
+        long long col = 0;
+        int nvalid = 0;
+        if (gs < TS) {
+            int lo = 0, hi = E;  // expert owning gs: the last g with s_sb[g] <= gs
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_sb[mid] <= gs) lo = mid; else hi = mid;
             }
+            const long long t0 = static_cast<long long>(s_start[lo]) + static_cast<long long>(gs - s_sb[lo]) * BK;
+            col = t0 >> 5;
+            const long long left = (static_cast<long long>(s_end[lo]) - t0 + 31) >> 5;
+            nvalid = static_cast<int>(left < 4 ? left : 4);
         }
-        const int off = (r & 31) * 16 + (r >> 5) * 4;
+        for (int r = warp; r < PREP_ROWS; r += PREP_THREADS / 32) {
+            const int row = row0 + r;
+            uint32_t wv = 0;
+            if (row < rows) {
+                const uint8_t* src = plane + static_cast<size_t>(row) * sM + col;
 #pragma unroll
-        for (int j = 0; j < PREP_STEPS_PER_TASK; ++j)
-            if (gsv[j] < TS) *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(gsv[j]) * dst_step + off) = w[j];
+                for (int kb = 0; kb < 4; ++kb)
+                    if (kb < nvalid) wv |= static_cast<uint32_t>(__ldg(src + kb)) << (8 * kb);
+            }
+            tile[r * (PREP_TILE_STEPS + 1) + lane] = wv;
+        }
+        __syncthreads();
+        // block j of this task: lane r0 writes rows r0, r0+32, r0+64, r0+96 (16 bytes)
+        for (int j = warp; j < PREP_TILE_STEPS; j += PREP_THREADS / 32) {
+            if (gs0 + j >= TS) continue;
+            uint4 o;
+            o.x = tile[(lane + 0) * (PREP_TILE_STEPS + 1) + j];
+            o.y = tile[(lane + 32) * (PREP_TILE_STEPS + 1) + j];
+            o.z = tile[(lane + 64) * (PREP_TILE_STEPS + 1) + j];
+            o.w = tile[(lane + 96) * (PREP_TILE_STEPS + 1) + j];
+            reinterpret_cast<uint4*>(dst + static_cast<size_t>(gs0 + j) * dst_step)[lane] = o;
+        }
+        __syncthreads();
     }
+    // This block's work is done: once every block got here the main kernel
+    // may launch and run its prologue (it waits for this grid's completion
+    // before reading anything written here). Triggering earlier would let its
+    // resident CTAs crowd this kernel off the SMs.
+    griddep_launch_dependents();
 }
 
 // ============================================================== main kernel
@@ -583,13 +597,14 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
 
     *what = "plan / scale re-layout kernel";
     {
-        // enough blocks for every task of the largest possible plan, at most 6 per SM
+        // enough blocks for every task of the largest possible plan, at most 4 per SM
         const long long tasks = static_cast<long long>(L.ntn + 2 * L.ntk) *
-                                ((L.ts_max + PREP_STEPS_PER_TASK - 1) / PREP_STEPS_PER_TASK);
-        long long blocks = (tasks + PREP_TASKS_PER_CTA - 1) / PREP_TASKS_PER_CTA;
-        if (blocks > 6LL * a.num_sms) blocks = 6LL * a.num_sms;
+                                ((L.ts_max + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS);
+        long long blocks = tasks;
+        if (blocks > 4LL * a.num_sms) blocks = 4LL * a.num_sms;
         if (blocks < 1) blocks = 1;
-        const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1);
+        const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
+                          sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
         wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(
             a.offs, a.sA, a.sB, plan, sfa, sfb, a.E, a.N, a.K, a.M, L.ts_max, L.ntn, L.ntk);
         cudaError_t e = cudaGetLastError();
