@@ -123,6 +123,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """Largest value over all ranks (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Replicas only: every rank processes the same workload, so the job does
+    world x the work in the slowest rank's time."""
+    return world * flop_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def make_device_inputs(name: str, device):
@@ -250,11 +269,7 @@ def bench_gpu(args):
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     main_ms = [a.elapsed_time(b) for a, b in evm]
-    total_ms = float(np.sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(np.sum(step_ms)), dist, device)
     assert mx.device_status(clear=True) == 0, "device flagged an error during the benchmark"
 
     # end to end through the public API with host buffers: H2D of every input,
@@ -285,7 +300,7 @@ def bench_gpu(args):
 
     flop = float(w.flop)
     ms_per_step = total_ms / K
-    value = world * flop / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(flop, world, ms_per_step)
     peak, peak_src, _ = mxfp8_peak()
     main_avg = float(np.mean(main_ms))
     achieved = flop / (main_avg * 1e-3) / 1e12

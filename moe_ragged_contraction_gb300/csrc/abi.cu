@@ -16,6 +16,7 @@ namespace {
 thread_local char g_err[512] = "no error";
 thread_local cudaEvent_t g_ev_before = nullptr;
 thread_local cudaEvent_t g_ev_after = nullptr;
+thread_local int g_stall_next = 0;
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -177,6 +178,8 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
         int K, int64_t M, uint16_t* out, void* ws, size_t ws_bytes, bool use_cache, void* stream) {
     cudaEvent_t evb = g_ev_before, eva = g_ev_after;
     g_ev_before = g_ev_after = nullptr;
+    const int stall = g_stall_next;
+    g_stall_next = 0;
     int rc = validate(A, sA, B, sB, offs, E, N, K, M, out);
     if (rc) return rc;
     if (E == 0) return MXFP8_OK;
@@ -218,6 +221,7 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     a.stream = st;
     a.ev_before = evb;
     a.ev_after = eva;
+    a.stall_first_stage = stall;
     const char* what = "";
     cudaError_t e = mxw::launch_wgrad(a, maps, &what);
     if (e != cudaSuccess) return fail_cuda(e, what);
@@ -268,6 +272,16 @@ int mxfp8_device_status(int32_t* status, int clear) {
     if (!status) return fail(MXFP8_EINVAL, "null status pointer");
     cudaError_t e = mxw::read_device_status(status, clear);
     if (e != cudaSuccess) return fail_cuda(e, "device status");
+    return MXFP8_OK;
+}
+
+// Failure-path test hook (not part of the public header): the next wgrad
+// call on this thread declares 16 more bytes than its first pipeline stage
+// receives, so that stage's wait can never complete and runs out after the
+// configured limit (MXFP8_WAIT_LIMIT_MS). The kernel then stops its pipeline,
+// sets MXFP8_DEV_WAIT_TIMEOUT and returns; nothing faults or hangs.
+int mxfp8_test_stall_next_call(int enable) {
+    g_stall_next = enable ? 1 : 0;
     return MXFP8_OK;
 }
 

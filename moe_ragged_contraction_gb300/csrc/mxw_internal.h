@@ -44,6 +44,7 @@ struct WgradArgs {
     uint64_t wait_limit_ns;
     cudaStream_t stream;
     cudaEvent_t ev_before, ev_after;
+    int stall_first_stage;  // failure-path test hook (0 in normal use)
 };
 
 // Rows of A and of B that one CTA loads per K-step (the CTA's half of a

@@ -265,6 +265,7 @@ struct MainParams {
     int E, N, K;
     int ts_max, ntn2, ntk;   // ntn2 = ceil(N / 256) pair-tile rows
     unsigned long long wait_ns;
+    int stall_first_stage;   // test hook: over-declare the first stage's bytes so its wait runs out
 };
 
 // Bounded wait: returns false (and raises the CTA's abort flag and the device
@@ -395,9 +396,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
                     const int st = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
+                    // test hook: only the (over-declared) first fill is issued, so the
+                    // stuck phase is never re-armed
+                    if (p.stall_first_stage && c >= 1) { ok = false; break; }
                     if (!wait_phase(bar_empty + 8 * st, ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
                     const uint32_t fb = full_leader + 8 * st;
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * st, PAIR_TX_BYTES);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * st, PAIR_TX_BYTES + (p.stall_first_stage ? 16u : 0u));
                     const int x = it.start + s * BK;
                     tma_load_2d_pair(sbase + OFF_A + st * A_STAGE, &tmA, fb, x, a_row);
                     tma_load_2d_pair(sbase + OFF_B + st * B_STAGE, &tmB, fb, x, b_row);
@@ -639,6 +643,7 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     mp.ntn2 = (a.N + PAIR_M - 1) / PAIR_M;
     mp.ntk = L.ntk;
     mp.wait_ns = a.wait_limit_ns;
+    mp.stall_first_stage = a.stall_first_stage;
     const long long total = static_cast<long long>(a.E) * mp.ntn2 * mp.ntk;
     const int pairs = static_cast<int>(total < max_pairs[a.dev] ? total : max_pairs[a.dev]);
     if (a.ev_before) {
