@@ -348,6 +348,85 @@ def bench_gpu(args):
     return result
 
 
+# ------------------------------------------------------------------ vendor comparators
+
+def bench_comparators(args):
+    """Opt-in context line: the same grouped wgrad in BF16 through the vendor
+    library (one cuBLAS GEMM per expert on its token slice; the pages compare
+    against a BF16 grouped GEMM, "Ragged MXFP8 Weight Gradients" section 7),
+    and a dense 8192^3 MXFP8 GEMM through this library (one expert) and
+    through cuBLASLt (torch._scaled_mm with e8m0 block scales; its scales are
+    not in the vendor's swizzled layout, so only its timing is meaningful)."""
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    device = torch.device("cuda")
+    mx.build()
+    mx.load()
+    w = I.WORKLOADS[args.config]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def timed(fn, steps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / steps
+
+    res = {"comparators": True, "config": {"workload": args.config}, "unit": "TFLOP/s"}
+    A, sA, B, sB, offs = make_device_inputs(args.config, device)
+    out = torch.empty((w.E, w.N, w.K), dtype=torch.bfloat16, device=device)
+    ms = timed(lambda: mx.wgrad_grouped(A, sA, B, sB, offs, out=out), args.steps)
+    res["mxfp8_wgrad_this_library"] = w.flop / (ms * 1e-3) / 1e12
+    # BF16 vendor baseline: one cuBLAS bf16 GEMM per expert on the token slice
+    # (torch._grouped_mm is not used: in PyTorch 2.9.1 for aarch64 its
+    # Blackwell kernel is built without TMEM support and fails at launch)
+    a16 = torch.randn(w.N, w.M, device=device, dtype=torch.bfloat16)
+    b16 = torch.randn(w.K, w.M, device=device, dtype=torch.bfloat16)
+    ends = I.offsets(I.group_sizes(args.config)).tolist()
+    out16 = torch.empty((w.E, w.N, w.K), dtype=torch.bfloat16, device=device)
+
+    def bf16_loop():
+        lo = 0
+        for g, hi in enumerate(ends):
+            if hi > lo:
+                torch.matmul(a16[:, lo:hi], b16[:, lo:hi].t(), out=out16[g])
+            else:
+                out16[g].zero_()
+            lo = hi
+
+    ms = timed(bf16_loop, args.steps)
+    res["bf16_per_expert_cublas"] = w.flop / (ms * 1e-3) / 1e12
+    res["mxfp8_over_bf16"] = res["mxfp8_wgrad_this_library"] / res["bf16_per_expert_cublas"]
+    n = 8192
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    qa, qsa = mx.quantize_tokenwise(torch.randn(n, n, device=device, generator=g))
+    qb, qsb = mx.quantize_tokenwise(torch.randn(n, n, device=device, generator=g))
+    one = torch.tensor([n], dtype=torch.int32, device=device)
+    dout = torch.empty((1, n, n), dtype=torch.bfloat16, device=device)
+    ms = timed(lambda: mx.wgrad_grouped(qa, qsa, qb, qsb, one, out=dout), args.steps)
+    res["dense8192_mxfp8_this_library"] = 2 * n ** 3 / (ms * 1e-3) / 1e12
+    try:
+        a8, b8 = qa.view(torch.float8_e4m3fn), qb.view(torch.float8_e4m3fn).t()
+        s_a, s_b = qsa.view(torch.float8_e8m0fnu), qsb.view(torch.float8_e8m0fnu)
+        ms = timed(lambda: torch._scaled_mm(a8, b8, scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16), args.steps)
+        res["dense8192_mxfp8_vendor"] = 2 * n ** 3 / (ms * 1e-3) / 1e12
+    except Exception as e:
+        res["dense8192_mxfp8_vendor"] = None
+        res["dense8192_vendor_error"] = str(e).splitlines()[0][:200]
+    return res
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 
 def _host_inputs(name: str):
@@ -415,10 +494,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--comparators", action="store_true",
+                    help="print a context line with vendor BF16 grouped / dense MXFP8 GEMM timings instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    res = bench_reference_arm(args) if args.impl == "reference" else bench_gpu(args)
+    if args.comparators:
+        res = bench_comparators(args)
+    else:
+        res = bench_reference_arm(args) if args.impl == "reference" else bench_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
