@@ -49,20 +49,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// As mbar_try_wait, acquiring at cluster scope (for phases completed by
-// arrivals from the peer CTA).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // ------------------------------------------------------------------ TMA / bulk copies
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -180,9 +166,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-// Arrive on an mbarrier in another CTA of the cluster.
+// Arrive on an mbarrier in another CTA of the cluster, with the default
+// (CTA-scope) release: it signals, it does not publish memory. (A
+// cluster-scope release would first wait for this thread's earlier global
+// stores to become visible cluster-wide, about a microsecond here.)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 2-D tiled load into this CTA's shared memory whose completion is counted on

@@ -271,14 +271,12 @@ struct MainParams {
 // Bounded wait: returns false (and raises the CTA's abort flag and the device
 // status word) if the phase does not complete within wait_ns, or returns
 // false at once if another role of this CTA already aborted.
-template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned long long wait_ns) {
-    auto done = [&] { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (done()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (done()) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > wait_ns) {
             *abort_flag = 1;
@@ -320,6 +318,18 @@ __device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int 
     it.nsteps = __ldg(ex + 4 * it.g + 2);
     it.step_base = __ldg(ex + 4 * it.g + 3);
     return it;
+}
+
+// Next item of this pair's static schedule at or after pass `pass` (which is
+// advanced past it), or -1 when the schedule is exhausted.
+__device__ __forceinline__ long long item_index(long long pass, int G, int pair);
+__device__ __forceinline__ long long next_item(long long& pass, int G, int pair, long long total) {
+    while (pass * G < total) {
+        const long long i = item_index(pass, G, pair);
+        ++pass;
+        if (i < total) return i;
+    }
+    return -1;
 }
 
 // Static schedule over CTA pairs: pass p hands items [p*G, (p+1)*G) to the
@@ -430,15 +440,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         if (leader) {
             uint32_t c = 0, tiles = 0;
             bool live = true;
-            for (long long pass = 0; pass * G < total; ++pass) {
-                const long long i = item_index(pass, G, pair);
-                if (i >= total) continue;
-                const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
+            // the next item's schedule entry is loaded one tile ahead, off the
+            // tile-boundary critical path
+            long long pass = 0;
+            long long i_next = next_item(pass, G, pair, total);
+            Item it_next = i_next >= 0 ? load_item(p.plan, p.E, p.ntk, nt_per_expert, i_next) : Item{};
+            while (i_next >= 0) {
+                const Item it = it_next;
+                i_next = next_item(pass, G, pair, total);
+                if (i_next >= 0) it_next = load_item(p.plan, p.E, p.ntk, nt_per_expert, i_next);
                 if (it.nsteps == 0) continue;
                 if (live) {
                     bool ok = true;
-                    // both CTAs' epilogues have drained the accumulator (peer arrivals are remote)
-                    if (lane == 0) ok = !*abort_flag && wait_phase<true>(bar_tempty, (tiles & 1) ^ 1, abort_flag, p.wait_ns);
+                    // both CTAs' epilogues have drained the accumulator; their arrivals
+                    // only signal (the drained TMEM loads completed before them), so a
+                    // CTA-scope acquire is enough
+                    if (lane == 0) ok = !*abort_flag && wait_phase(bar_tempty, (tiles & 1) ^ 1, abort_flag, p.wait_ns);
                     live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 }
                 tc_fence_after();
