@@ -62,6 +62,9 @@ cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_
 // Sets the calling thread's mxfp8_last_error() message; returns `code`.
 int set_last_error(int code, const char* msg);
 
+// Suspend hint (ns) for the kernels' mbarrier waits on the current device.
+cudaError_t set_suspend_hint(uint32_t ns);
+
 // Device status word (MXFP8_DEV_* bits).
 cudaError_t read_device_status(int32_t* status, int clear);
 

@@ -271,12 +271,15 @@ struct MainParams {
 // Bounded wait: returns false (and raises the CTA's abort flag and the device
 // status word) if the phase does not complete within wait_ns, or returns
 // false at once if another role of this CTA already aborted.
+__device__ uint32_t g_suspend_ns = 0;  // try_wait suspend hint for waiting roles (0: plain polling)
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned long long wait_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint32_t hint = g_suspend_ns;
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (hint ? mbar_try_wait_suspend(bar, parity, hint) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > wait_ns) {
             *abort_flag = 1;
@@ -690,6 +693,8 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     }
     return cudaSuccess;
 }
+
+cudaError_t set_suspend_hint(uint32_t ns) { return cudaMemcpyToSymbol(g_suspend_ns, &ns, sizeof(ns)); }
 
 cudaError_t read_device_status(int32_t* status, int clear) {
     cudaError_t e = cudaDeviceSynchronize();
