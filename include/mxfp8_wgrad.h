@@ -98,7 +98,8 @@ int mxfp8_wgrad_grouped(const uint8_t* A, const uint8_t* sA, const uint8_t* B, c
                         void* stream);
 
 /* Bytes of scratch that mxfp8_wgrad_grouped_ws needs for these sizes (an upper
- * bound over every routing of M tokens into E groups). 0 if the sizes are
+ * bound over every routing of M tokens into E groups and over both tile
+ * orientations, for the current tile-width setting). 0 if the sizes are
  * invalid. Host-only, no CUDA call. */
 size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M);
 
@@ -166,6 +167,35 @@ int mxfp8_device_status(int32_t* status, int clear);
 int mxfp8_wgrad_grouped_noalloc(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                                 const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
                                 void* stream);
+
+/*
+ * Output tiling. One CTA pair (two SMs) owns a 256 x TN tile of one expert's
+ * output for the expert's whole token run. The 256-row side runs over the rows
+ * of A (output rows n, TN over output columns k) or over the rows of B (output
+ * columns k, TN over output rows n; the tile is then accumulated transposed
+ * and stored back transposed). TN is a multiple of 16 up to 448. By default
+ * the library picks the orientation and TN from a cost model of its kernel
+ * (operand bytes per step against tensor-core cycles, padding and tile count).
+ * The arithmetic per output element is the same for every tiling: results are
+ * identical bit for bit across orientations and tile widths.
+ *
+ * mxfp8_wgrad_set_tile_orientation(mode) sets the orientation for the process
+ * (every thread, every later call): 0 = automatic, 1 = 256 side on A,
+ * 2 = 256 side on B. The initial mode comes from the environment variable
+ * MXFP8_TILE_ORIENTATION ("auto", "nk" = 1, "kn" = 2), read at the first call.
+ * mxfp8_wgrad_set_tile_rows(tn) forces TN (a multiple of 16 in [16, 448]) or
+ * returns to the modelled choice (0). Both return MXFP8_EINVAL for other
+ * values. mxfp8_wgrad_workspace_bytes follows the current settings: change
+ * them before sizing a workspace.
+ *
+ * mxfp8_wgrad_tile_config(E, N, K, M, ...) reports the tiling the current
+ * settings give for these sizes: *kn = 1 when the 256 side is on B, *tn = TN,
+ * and the tile counts along the 256 side and the TN side. Host-only, no CUDA
+ * call.
+ */
+int mxfp8_wgrad_set_tile_orientation(int mode);
+int mxfp8_wgrad_set_tile_rows(int tn);
+int mxfp8_wgrad_tile_config(int E, int N, int K, int64_t M, int* kn, int* tn, int* tiles_m, int* tiles_n);
 
 /* Measurement hook: when both events are non-NULL, the next
  * mxfp8_wgrad_grouped{,_ws} call on this thread records `ev_before` on its

@@ -13,7 +13,10 @@ from ._lib import (  # noqa: F401
     lib_path,
     load,
     quantize_tokenwise,
+    set_tile_orientation,
+    set_tile_rows,
     set_timing_events,
+    tile_config,
     wgrad_grouped,
     workspace_bytes,
 )

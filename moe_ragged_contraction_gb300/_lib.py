@@ -66,6 +66,13 @@ def load() -> ctypes.CDLL:
         lib.mxfp8_device_status.restype = I
         lib.mxfp8_wgrad_set_timing_events.argtypes = [P, P]
         lib.mxfp8_wgrad_set_timing_events.restype = I
+        lib.mxfp8_wgrad_set_tile_orientation.argtypes = [I]
+        lib.mxfp8_wgrad_set_tile_orientation.restype = I
+        IP = ctypes.POINTER(ctypes.c_int)
+        lib.mxfp8_wgrad_set_tile_rows.argtypes = [I]
+        lib.mxfp8_wgrad_set_tile_rows.restype = I
+        lib.mxfp8_wgrad_tile_config.argtypes = [I, I, I, L, IP, IP, IP, IP]
+        lib.mxfp8_wgrad_tile_config.restype = I
         _lib = lib
         return lib
 
@@ -137,6 +144,27 @@ def wgrad_grouped(A, sA, B, sB, offs, out=None, workspace=None, stream=None):
 
 def workspace_bytes(E: int, N: int, K: int, M: int) -> int:
     return int(load().mxfp8_wgrad_workspace_bytes(E, N, K, M))
+
+
+ORIENT_AUTO, ORIENT_NK, ORIENT_KN = 0, 1, 2
+
+
+def set_tile_orientation(mode: int) -> None:
+    """Process-wide tile orientation: 0 automatic, 1 (256-row side on A), 2 (on B)."""
+    check(load().mxfp8_wgrad_set_tile_orientation(int(mode)))
+
+
+def set_tile_rows(tn: int) -> None:
+    """Process-wide N-side tile width: 0 for the modelled choice, else a multiple of 16 in [16, 448]."""
+    check(load().mxfp8_wgrad_set_tile_rows(int(tn)))
+
+
+def tile_config(E: int, N: int, K: int, M: int) -> dict:
+    """Tiling the current settings give for E experts, an [N, K] output and M tokens."""
+    v = [ctypes.c_int(0) for _ in range(4)]
+    check(load().mxfp8_wgrad_tile_config(E, N, K, M, *(ctypes.byref(x) for x in v)))
+    kn, tn, tm, tnn = (int(x.value) for x in v)
+    return {"kn": kn, "tn": tn, "tiles_m": tm, "tiles_n": tnn}
 
 
 def quantize_tokenwise(x, q=None, s=None, stream=None):

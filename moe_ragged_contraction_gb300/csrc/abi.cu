@@ -4,6 +4,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 #include <vector>
@@ -149,6 +150,40 @@ int cached_workspace(int dev, cudaStream_t stream, size_t need, void** out) {
     return MXFP8_OK;
 }
 
+// Tile orientation mode (mxfp8_wgrad_set_tile_orientation); the initial value
+// comes from MXFP8_TILE_ORIENTATION ("auto", "nk" or "kn"; default auto).
+std::atomic<int> g_orientation{-1};
+// N-side tile rows forced by mxfp8_wgrad_set_tile_rows (0 = modelled best);
+// the initial value comes from MXFP8_TILE_ROWS (ignored unless admissible).
+std::atomic<int> g_tile_rows{-1};
+
+int orientation_mode() {
+    int m = g_orientation.load(std::memory_order_relaxed);
+    if (m < 0) {
+        const char* s = getenv("MXFP8_TILE_ORIENTATION");
+        int v = 0;
+        if (s && (s[0] == 'n' || s[0] == 'N')) v = 1;
+        if (s && (s[0] == 'k' || s[0] == 'K')) v = 2;
+        int expected = -1;
+        g_orientation.compare_exchange_strong(expected, v);
+        m = g_orientation.load(std::memory_order_relaxed);
+    }
+    return m;
+}
+
+int tile_rows_setting() {
+    int t = g_tile_rows.load(std::memory_order_relaxed);
+    if (t < 0) {
+        const char* s = getenv("MXFP8_TILE_ROWS");
+        int v = s ? atoi(s) : 0;
+        if (v < 16 || v > mxw::MAX_TN || v % 16 != 0) v = 0;
+        int expected = -1;
+        g_tile_rows.compare_exchange_strong(expected, v);
+        t = g_tile_rows.load(std::memory_order_relaxed);
+    }
+    return t;
+}
+
 uint64_t wait_limit_ns() {
     static uint64_t v = [] {
         const char* s = getenv("MXFP8_WAIT_LIMIT_MS");
@@ -183,13 +218,19 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     int rc = validate(A, sA, B, sB, offs, E, N, K, M, out);
     if (rc) return rc;
     if (E == 0) return MXFP8_OK;
+    mxw::TileConfig tc;
     mxw::WsLayout lay;
-    if (!mxw::ws_layout(E, N, K, M, &lay)) return fail(MXFP8_EINVAL, "unsupported sizes");
+    if (!mxw::choose_tiles(N, K, E, M, orientation_mode(), tile_rows_setting(), &tc) ||
+        !mxw::ws_layout(E, N, K, M, tc, &lay))
+        return fail(MXFP8_EINVAL, "unsupported sizes");
     if (!use_cache) {
         if (!ws) return fail(MXFP8_EINVAL, "null workspace");
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MXFP8_EALIGN, "workspace must be 256-byte aligned");
-        if (ws_bytes < lay.total)
-            return fail(MXFP8_ENOWS, "workspace of %zu bytes, need %zu", ws_bytes, lay.total);
+        // the documented requirement (the bound over both orientations), not just
+        // this call's layout, so that a size that works once works for any routing
+        const size_t need = mxw::ws_bytes_any_orientation(E, N, K, M, tile_rows_setting());
+        if (ws_bytes < need || ws_bytes < lay.total)
+            return fail(MXFP8_ENOWS, "workspace of %zu bytes, need %zu", ws_bytes, need > lay.total ? need : lay.total);
     }
     int dev;
     DeviceInfo info;
@@ -215,14 +256,22 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
         rc = cached_workspace(dev, st, lay.total, &ws);
         if (rc) return rc;
     }
-    CUtensorMap maps[4];
-    rc = make_operand_map(&maps[0], A, N, M, mxw::HALF_TILE_ROWS);
+    // M side: 256-row pair tiles, 128 rows per CTA; N side: tn-row tiles, per CTA
+    // n1/2 rows for the first MMA and n2/2 for the second
+    CUtensorMap maps[5];
+    const uint8_t* m_op = tc.kn ? B : A;
+    const uint8_t* n_op = tc.kn ? A : B;
+    const int n_rows = tc.kn ? N : K;
+    rc = make_operand_map(&maps[0], m_op, tc.kn ? K : N, M, mxw::BM);
     if (rc) return rc;
-    rc = make_operand_map(&maps[1], B, K, M, mxw::HALF_TILE_ROWS);
+    rc = make_operand_map(&maps[1], n_op, n_rows, M, tc.n1 / 2);
     if (rc) return rc;
-    rc = make_sf_map(&maps[2], static_cast<uint8_t*>(ws) + lay.sfa_off, static_cast<int64_t>(lay.ntn) * lay.ts_max, 1);
+    rc = make_operand_map(&maps[2], n_op, n_rows, M, tc.n2 ? tc.n2 / 2 : tc.n1 / 2);
     if (rc) return rc;
-    rc = make_sf_map(&maps[3], static_cast<uint8_t*>(ws) + lay.sfb_off, static_cast<int64_t>(lay.ntk) * lay.ts_max * 2, 2);
+    rc = make_sf_map(&maps[3], static_cast<uint8_t*>(ws) + lay.sfm_off, static_cast<int64_t>(tc.tiles_m) * lay.ts_max * 2, 1);
+    if (rc) return rc;
+    rc = make_sf_map(&maps[4], static_cast<uint8_t*>(ws) + lay.sfn_off,
+                     static_cast<int64_t>(tc.tiles_n) * lay.ts_max * tc.nblk_n, tc.nblk_n);
     if (rc) return rc;
 
     mxw::WgradArgs a;
@@ -255,9 +304,32 @@ int mxfp8_wgrad_grouped(const uint8_t* A, const uint8_t* sA, const uint8_t* B, c
 }
 
 size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M) {
-    mxw::WsLayout lay;
-    if (!mxw::ws_layout(E, N, K, M, &lay)) return 0;
-    return lay.total;
+    return mxw::ws_bytes_any_orientation(E, N, K, M, tile_rows_setting());
+}
+
+int mxfp8_wgrad_set_tile_orientation(int mode) {
+    if (mode < 0 || mode > 2) return fail(MXFP8_EINVAL, "tile orientation mode %d not in {0, 1, 2}", mode);
+    g_orientation.store(mode, std::memory_order_relaxed);
+    return MXFP8_OK;
+}
+
+int mxfp8_wgrad_set_tile_rows(int tn) {
+    if (tn != 0 && (tn < 16 || tn > mxw::MAX_TN || tn % 16 != 0))
+        return fail(MXFP8_EINVAL, "tile rows %d: 0 or a multiple of 16 in [16, %d]", tn, mxw::MAX_TN);
+    g_tile_rows.store(tn, std::memory_order_relaxed);
+    return MXFP8_OK;
+}
+
+int mxfp8_wgrad_tile_config(int E, int N, int K, int64_t M, int* kn, int* tn, int* tiles_m, int* tiles_n) {
+    mxw::TileConfig tc;
+    if (!kn || !tn || !tiles_m || !tiles_n) return fail(MXFP8_EINVAL, "null pointer argument");
+    if (!mxw::choose_tiles(N, K, E, M, orientation_mode(), tile_rows_setting(), &tc))
+        return fail(MXFP8_EINVAL, "N=%d and K=%d must be >= 1", N, K);
+    *kn = tc.kn;
+    *tn = tc.tn;
+    *tiles_m = tc.tiles_m;
+    *tiles_n = tc.tiles_n;
+    return MXFP8_OK;
 }
 
 int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,

@@ -8,12 +8,12 @@
 
 namespace mxw {
 
-// Output tile of one CTA: BM rows of A (the N axis) x BN rows of B (the K
-// axis); the token axis is walked in K-steps of BK tokens ("Ragged MXFP8
-// Weight Gradients", section 1: a pipelined kernel walks the contraction in
-// fixed steps of 128 tokens along M).
+// A CTA pair owns a 256 x TN output tile (TN <= MAX_TN); the token axis is
+// walked in K-steps of BK tokens ("Ragged MXFP8 Weight Gradients", section 1:
+// a pipelined kernel walks the contraction in fixed steps of 128 tokens along
+// M). BM is the share of one CTA of the pair's 256 "M-side" rows.
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int MAX_TN = 448;
 constexpr int BK = 128;
 constexpr int SF_ATOM = 512;  // bytes of scale factors for 128 rows x one K-step
 
@@ -23,14 +23,37 @@ constexpr int SF_ATOM = 512;  // bytes of scale factors for 128 rows x one K-ste
 //   [PLAN_HDR + 4E + r]        = expert with the r-th longest token run.
 constexpr int PLAN_HDR = 8;
 
-struct WsLayout {
-    size_t plan_off, sfa_off, sfb_off, total;
-    int ts_max;  // upper bound on the total number of K-steps
-    int ntn, ntk;
+// Tile orientation and sizes. kn == 0: the pair's 256-row "M side" runs over
+// the rows of A (output rows n) and the TN-row "N side" over the rows of B
+// (output columns k); kn == 1 swaps them (the accumulator then holds the tile
+// transposed). tn = n1 + n2: the widths of the one or two MMAs per 32-token
+// chunk (n1 = min(tn, 256)); nblk_n = ceil(tn / 128) scale blocks per N-side
+// tile; tiles_m = ceil(rows of the M side / 256), tiles_n = ceil(rows of the
+// N side / tn).
+struct TileConfig {
+    int kn, tn, n1, n2, nblk_n, tiles_m, tiles_n;
 };
 
-// Workspace layout for these sizes; returns false if the sizes are invalid.
-bool ws_layout(int E, int N, int K, int64_t M, WsLayout* out);
+// force: 0 = the orientation the kernel's cost model prefers (ties: kn == 0),
+// 1 = kn == 0, 2 = kn == 1. force_tn: 0 = the modelled best tn of that
+// orientation, else that tn (a multiple of 16 in [16, MAX_TN]). E and M (the
+// mean run length) weigh the per-tile overhead. Returns false for invalid
+// sizes or an invalid force_tn.
+bool choose_tiles(int N, int K, int E, int64_t M, int force, int force_tn, TileConfig* tc);
+
+// Workspace: the plan, then the M side's scale-factor blocks
+// [tiles_m][ts_max][2][512 B], then the N side's [tiles_n][ts_max][nblk_n][512 B].
+struct WsLayout {
+    size_t plan_off, sfm_off, sfn_off, total;
+    int ts_max;  // upper bound on the total number of K-steps
+    TileConfig tc;
+};
+
+// Workspace layout for these sizes and tiles; returns false if unsupported.
+bool ws_layout(int E, int N, int K, int64_t M, const TileConfig& tc, WsLayout* out);
+
+// Largest workspace over both orientations (0 if the sizes are invalid).
+size_t ws_bytes_any_orientation(int E, int N, int K, int64_t M, int force_tn);
 
 struct WgradArgs {
     const uint8_t *A, *sA, *B, *sB;
@@ -47,14 +70,12 @@ struct WgradArgs {
     int stall_first_stage;  // failure-path test hook (0 in normal use)
 };
 
-// Rows of A and of B that one CTA loads per K-step (the CTA's half of a
-// 256 x 256 pair tile).
-constexpr int HALF_TILE_ROWS = 128;
-
 // Enqueue the plan / scale re-layout kernel and the main contraction kernel.
-// maps: A and B operand tiles (HALF_TILE_ROWS rows x BK tokens, 128-byte
-// swizzle) and the scale-factor workspaces viewed as u32 [blocks][128]
-// (boxes of 1 and 2 blocks). Returns a cudaError_t; `what` names the step.
+// maps: the M-side operand (boxes of BM rows x BK tokens), the N-side operand
+// for the first and the second MMA (n1/2 and n2/2 rows x BK tokens; the second
+// is unused when n2 == 0), all with the 128-byte swizzle, and the two sides'
+// scale-factor blocks viewed as u32 [blocks][128] (boxes of 1 and nblk_n
+// blocks). Returns a cudaError_t; `what` names the step.
 cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what);
 
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream);

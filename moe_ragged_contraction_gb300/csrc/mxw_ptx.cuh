@@ -161,6 +161,15 @@ __device__ __forceinline__ void reg_fence(uint32_t (&v)[32]) {
 }
 
 
+// Returns x through an opaque register move, so that the compiler keeps the
+// value in a register instead of re-reading it (e.g. a kernel parameter from
+// the constant bank) where it is used.
+__device__ __forceinline__ uint32_t in_reg(uint32_t x) {
+    uint32_t r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 // ------------------------------------------------------------------ clusters / CTA pairs
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

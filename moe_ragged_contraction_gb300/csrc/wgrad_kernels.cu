@@ -4,8 +4,8 @@
 //   section 1  — dW[g] = dY[g]^T X[g]; offsets cut the contraction (token) axis;
 //                A = dY^T [N,M], B = X^T [K,M] token-contiguous E4M3, one E8M0
 //                scale per 32 tokens in planes [N,M/32] and [K,M/32];
-//   section 4  — one CTA owns an output tile for its whole reduction (no
-//                atomics, bit-reproducible);
+//   section 4  — one CTA (here: one CTA pair) owns an output tile for its whole
+//                reduction (no atomics, bit-reproducible);
 //   section 5.3 — ragged runs: runtime length, 32-aligned start, empty experts
 //                get an explicit zero store, scale reads stay in bounds;
 //   section 5.4 — longest-expert-first order shortens the tail;
@@ -15,14 +15,21 @@
 // Two kernels per call:
 //   wgrad_prep : reads offs, clamps them, builds the schedule (per-expert
 //                start / length / K-steps, longest-first order) and gathers
-//                the scale bytes of every (128-row block, K-step) into the
-//                512-byte tcgen05 scale-factor block layout.
-//   wgrad_main : persistent, warp-specialised: warp 0 issues TMA loads of the
-//                A/B K-step tiles and bulk copies of their scale blocks into
-//                a STAGES-deep shared-memory ring; warp 1 copies scales to
-//                TMEM and issues tcgen05.mma kind::mxf8f6f4 block-scaled MMAs
-//                into a 128x256 fp32 TMEM accumulator; warps 2-9 drain TMEM,
-//                narrow to bf16 and store.
+//                the scale bytes of every (128-row block of a tile, K-step)
+//                into the 512-byte tcgen05 scale-factor block layout.
+//   wgrad_main : persistent CTA pairs (2-CTA clusters, cta_group::2 MMAs),
+//                warp-specialised: TMA producer, MMA issuer, stage watcher and
+//                8 epilogue warps per CTA.
+//
+// Tiling. A pair tile is 256 rows of the "M-side" operand (split 128 / 128
+// over the two CTAs and over TMEM lanes) by TN rows of the "N-side" operand
+// (TN a multiple of 16, at most 448). Each 32-token chunk is one MMA of
+// N1 = min(TN, 256) columns plus, for TN > 256, a second of N2 = TN - 256
+// columns into the next TMEM columns; each CTA holds half of either MMA's
+// N-side rows. The host picks which operand is the M side (A, rows n, by
+// default; or B, rows k, the accumulator then holding the tile transposed)
+// and TN from a cost model of the kernel (operand bytes per K-step against
+// MMA cycles, padding, tile count).
 //
 // A K-step starts exactly at the group's first token (TMA coordinates need
 // only 16-byte alignment, and 32 tokens are 32 bytes), so there is no leading
@@ -43,18 +50,23 @@ constexpr int PREP_THREADS = 256;
 constexpr int PREP_ROWS = 128;        // rows of one scale-factor block
 constexpr int PREP_TILE_STEPS = 32;   // K-steps per gather task (one per lane)
 
+struct PrepSide {
+    const uint8_t* plane;  // scale plane [rows][M/32]
+    uint8_t* sf;           // scale-factor blocks [tiles][ts_max][blocks][512 B]
+    int rows, tile_rows, tiles;
+    int blocks;            // 128-row blocks per tile: ceil(tile_rows / 128)
+};
+
 // Every block first rebuilds the per-expert runs from offs (one warp, shuffle
 // scans; 3E + 1 words of shared memory). Block 0 also writes the plan. Then
 // the blocks stride over gather tasks (below), writing the 512-byte
-// scale-factor blocks, where row r, 32-token block kb sits at byte
-// (r % 32) * 16 + (r / 32) * 4 + kb. Row blocks: A's ceil(N/128) first, then
-// B's, two per 256-row B tile.
-__global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs,
-                                                           const uint8_t* __restrict__ sA,
-                                                           const uint8_t* __restrict__ sB,
-                                                           int32_t* __restrict__ plan, uint8_t* __restrict__ sfa,
-                                                           uint8_t* __restrict__ sfb, int E, int N, int K,
-                                                           long long M, int ts_max, int ntn, int ntk) {
+// scale-factor blocks: block h of tile t of a side holds rows
+// t * tile_rows + 128 h + r (r < 128; zero past the tile or the plane), and
+// row r, 32-token block kb sits at byte (r % 32) * 16 + (r / 32) * 4 + kb.
+// Blocks: the M side's tiles * blocks first, then the N side's.
+__global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs, const PrepSide sm_side,
+                                                           const PrepSide sn_side, int32_t* __restrict__ plan, int E,
+                                                           long long M, int ts_max) {
     extern __shared__ int prep_smem[];
     int* s_start = prep_smem;        // [E]
     int* s_end = s_start + E;        // [E]
@@ -134,33 +146,27 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         }
     }
 
-    // Scale-factor gather as a tile transpose: a task is (128-row block rb,
-    // 32 consecutive global K-steps). Lane l of a warp owns K-step gs0 + l and
+    // Scale-factor gather as a tile transpose: a task is (128-row block, 32
+    // consecutive global K-steps). Lane l of a warp owns K-step gs0 + l and
     // loads that step's 4 scale bytes of one row, so consecutive lanes read
     // consecutive 4-byte groups of the row (coalesced within an expert); the
     // words are staged in a padded [128][33] shared tile, then each 512-byte
     // block is written by one warp with 16-byte stores.
     uint32_t* tile = reinterpret_cast<uint32_t*>(s_sb + E + 1);  // [PREP_ROWS][PREP_TILE_STEPS + 1]
     const int nchunks = (TS + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS;
-    const long long ntasks = static_cast<long long>(ntn + 2 * ntk) * nchunks;
+    const int mblocks = sm_side.tiles * sm_side.blocks;
+    const int nblk = mblocks + sn_side.tiles * sn_side.blocks;
+    const long long ntasks = static_cast<long long>(nblk) * nchunks;
     const long long sM = M / 32;
     for (long long task = blockIdx.x; task < ntasks; task += gridDim.x) {
-        const int rb = static_cast<int>(task / nchunks);
-        const int gs0 = static_cast<int>(task - static_cast<long long>(rb) * nchunks) * PREP_TILE_STEPS;
-        const uint8_t* plane;
-        int rows, row0;
-        uint8_t* dst;       // scale-factor block of global K-step 0 for this row block
-        size_t dst_step;    // bytes between consecutive global K-steps
-        if (rb < ntn) {
-            plane = sA; rows = N; row0 = rb * BM;
-            dst = sfa + static_cast<size_t>(rb) * ts_max * SF_ATOM;
-            dst_step = SF_ATOM;
-        } else {
-            const int rbb = rb - ntn;
-            plane = sB; rows = K; row0 = rbb * BM;
-            dst = sfb + (static_cast<size_t>(rbb >> 1) * ts_max * 2 + (rbb & 1)) * SF_ATOM;
-            dst_step = 2 * SF_ATOM;
-        }
+        const int hb = static_cast<int>(task / nchunks);
+        const int gs0 = static_cast<int>(task - static_cast<long long>(hb) * nchunks) * PREP_TILE_STEPS;
+        const bool mside = hb < mblocks;
+        const PrepSide& sd = mside ? sm_side : sn_side;
+        const int local = mside ? hb : hb - mblocks;
+        const int t = local / sd.blocks, h = local - t * sd.blocks;
+        const int in_tile0 = PREP_ROWS * h;  // first row of this block inside its tile
+        const int row0 = t * sd.tile_rows + in_tile0;
         // this lane's K-step: its expert, first scale column and valid 32-token blocks
         const int gs = gs0 + lane;
         long long col = 0;
@@ -179,8 +185,8 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         for (int r = warp; r < PREP_ROWS; r += PREP_THREADS / 32) {
             const int row = row0 + r;
             uint32_t wv = 0;
-            if (row < rows) {
-                const uint8_t* src = plane + static_cast<size_t>(row) * sM + col;
+            if (in_tile0 + r < sd.tile_rows && row < sd.rows) {
+                const uint8_t* src = sd.plane + static_cast<size_t>(row) * sM + col;
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb)
                     if (kb < nvalid) wv |= static_cast<uint32_t>(__ldg(src + kb)) << (8 * kb);
@@ -196,7 +202,8 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
             o.y = tile[(lane + 32) * (PREP_TILE_STEPS + 1) + j];
             o.z = tile[(lane + 64) * (PREP_TILE_STEPS + 1) + j];
             o.w = tile[(lane + 96) * (PREP_TILE_STEPS + 1) + j];
-            reinterpret_cast<uint4*>(dst + static_cast<size_t>(gs0 + j) * dst_step)[lane] = o;
+            uint8_t* dst = sd.sf + ((static_cast<size_t>(t) * ts_max + gs0 + j) * sd.blocks + h) * SF_ATOM;
+            reinterpret_cast<uint4*>(dst)[lane] = o;
         }
         __syncthreads();
     }
@@ -209,33 +216,28 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
 
 // ============================================================== main kernel
 
-// One CTA pair (a 2-CTA cluster) owns a 256 x 256 output tile: rows
-// [nt*256, nt*256+256) of A (the N axis) by rows [kt*256, kt*256+256) of B
-// (the K axis). CTA r of the pair holds A rows nt*256 + 128r .. +128 and B
-// rows kt*256 + 128r .. +128 in its shared memory, its own 128 accumulator
-// rows in its TMEM, and stores those 128 output rows. The leader (r = 0)
-// issues the M = 256 block-scaled MMAs for both; each SM then reads 32 KB of
-// operands per K-step instead of the 48 KB a 128 x 256 single-CTA tile needs.
-constexpr int PAIR_M = 2 * BM;    // 256 rows of A per pair tile
-constexpr int HALF_N = BN / 2;    // 128 rows of B per CTA
-constexpr int STAGES = 6;
-constexpr int A_STAGE = BM * BK;       // 16 KB
-constexpr int B_STAGE = HALF_N * BK;   // 16 KB
-constexpr int SFA_STAGE = SF_ATOM;     // this CTA's 128 A rows
-constexpr int SFB_STAGE = 2 * SF_ATOM; // all 256 B rows of the tile (each CTA's MMA half needs them)
-constexpr uint32_t CTA_TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
-constexpr uint32_t PAIR_TX_BYTES = 2 * CTA_TX_BYTES;
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], tmem_full, tmem_empty, drain
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int MAIN_SMEM = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+// One CTA pair (a 2-CTA cluster) owns a 256 x TN output tile. CTA r of the
+// pair holds M-side rows tm*256 + 128r .. +128 and half of the N-side rows of
+// each MMA (rows r*N1/2 .. +N1/2 and N1 + r*N2/2 .. +N2/2 of the tile) in its
+// shared memory, its own 128 accumulator rows in its TMEM, and stores those
+// 128 rows of the tile. The leader (r = 0) issues the M = 256 block-scaled
+// MMAs for both; each SM then reads 16 KB + TN * 64 bytes of operands per
+// K-step for 128 x TN x 128 multiply-adds.
+//
+// Shared memory (runtime-sized rings of `stages` entries, each 1024-byte
+// aligned where the 128-byte swizzle needs it): M-side tiles [stages][16 KB],
+// N-side tiles [stages][TN/2 * 128 B], M-side scale blocks [stages][512 B],
+// N-side scale blocks [stages][nblk_n * 512 B], then the mbarriers.
+// TMEM (512 columns): accumulator columns [0, TN); from column TN on,
+// `sf_slots` scale-factor slots of 4 + 4 * nblk_n columns (M-side block,
+// then the N-side blocks).
+constexpr int PAIR_M = 2 * BM;        // 256 M-side rows per pair tile
+constexpr int A_STAGE = BM * BK;      // M-side operand: this CTA's 128 rows (16 KB)
 constexpr int EPI_WARPS = 8;
-constexpr int MAIN_THREADS = 32 * (3 + EPI_WARPS);  // producer, MMA issuer, stage watcher, epilogue
+constexpr int EPI_WARP0 = 3;                        // producer, MMA issuer, stage watcher, then the epilogue
+constexpr int MAIN_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+constexpr int MAX_STAGES = 7;
+constexpr int MAIN_SMEM_MAX = 232448;  // the sm_100-family opt-in limit per CTA
 // Named barriers between the stage watcher and the MMA warp (64 threads each):
 // BAR_READY + st: stage st holds data (watcher arrives, MMA warp syncs);
 // BAR_FREE + st: the MMA warp has taken stage st (MMA warp arrives, watcher
@@ -244,35 +246,36 @@ constexpr int MAIN_THREADS = 32 * (3 + EPI_WARPS);  // producer, MMA issuer, sta
 constexpr uint32_t BAR_READY = 1;
 constexpr uint32_t BAR_FREE = 8;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_SFA = 256;  // + 4 * stage: 4 columns of A scales per stage
-constexpr uint32_t TMEM_SFB = 288;  // + 8 * stage: 8 columns of B scales per stage
 
-static_assert(OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(TMEM_SFA + 4 * STAGES <= TMEM_SFB && TMEM_SFB + 8 * STAGES <= TMEM_COLS, "TMEM budget");
-static_assert(MAIN_SMEM <= 232448, "shared memory budget");
-static_assert(BAR_READY + STAGES <= BAR_FREE && BAR_FREE + STAGES <= 16, "named barrier ids");
+static_assert(BAR_READY + MAX_STAGES <= BAR_FREE && BAR_FREE + MAX_STAGES <= 16, "named barrier ids");
+static_assert(MAX_TN <= 448 && MAX_TN % 16 == 0, "N-side tile: at most two MMAs (256 + 192 columns)");
 
 // Instruction descriptor, kind::mxf8f6f4: A and B E4M3 (0), both K-major,
-// N >> 3 at bits 17-22, E8M0 scales (bit 23), M >> 4 at bits 24-28 (M = 256
-// across the pair); the scale byte selectors for B (bits 4-5) and A (bits
-// 29-30) are or-ed in per MMA.
-constexpr uint32_t IDESC_BASE = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-                                (static_cast<uint32_t>(PAIR_M >> 4) << 24);
+// E8M0 scales (bit 23), M >> 4 at bits 24-28 (M = 256 across the pair). N >> 3
+// (bits 17-22) is or-ed in per MMA width, the scale byte selectors for B
+// (bits 4-5) and A (bits 29-30) per 32-token chunk.
+constexpr uint32_t IDESC_BASE = (1u << 23) | (static_cast<uint32_t>(PAIR_M >> 4) << 24);
 
 struct MainParams {
     const int32_t* plan;
     uint16_t* out;
-    int E, N, K;
-    int ts_max, ntn2, ntk;   // ntn2 = ceil(N / 256) pair-tile rows
+    int E, N, K;             // out[E][N][K]
+    int ts_max;
+    int tiles_m, tiles_n;    // pair tiles along the M side (256 rows) and the N side (tn rows)
+    int tn, n1, n2;          // N-side tile rows = n1 + n2 (the two MMA widths; n2 may be 0)
+    int nblk_n;              // 128-row scale blocks per N-side tile
+    int kn;                  // 0: M side = rows of A (n), N side = rows of B (k); 1: swapped
+    int stages, sf_slots;
+    uint32_t off_b, off_sfa, off_sfb, off_bar, b_stage;  // shared-memory layout (bytes)
     unsigned long long wait_ns;
     int stall_first_stage;   // test hook: over-declare the first stage's bytes so its wait runs out
 };
 
+__device__ uint32_t g_suspend_ns = 0;  // try_wait suspend hint for waiting roles (0: plain polling)
+
 // Bounded wait: returns false (and raises the CTA's abort flag and the device
 // status word) if the phase does not complete within wait_ns, or returns
 // false at once if another role of this CTA already aborted.
-__device__ uint32_t g_suspend_ns = 0;  // try_wait suspend hint for waiting roles (0: plain polling)
-
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned long long wait_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -301,12 +304,12 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, unsig
 }
 
 struct Item {
-    int g, nt, kt, start, len, nsteps, step_base;
+    int g, tm, tn, start, len, nsteps, step_base;
 };
 
 // Work item i (in longest-expert-first order, the tiles of one expert
-// consecutive, K-tiles fastest) -> expert and pair tile.
-__device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int E, int ntk, int nt_per_expert,
+// consecutive, N-side tiles fastest) -> expert and pair tile.
+__device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int E, int tiles_n, int nt_per_expert,
                                           long long i) {
     const int32_t* ex = plan + PLAN_HDR;
     const int32_t* order = ex + 4 * E;
@@ -314,25 +317,13 @@ __device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int 
     const int t = static_cast<int>(i - static_cast<long long>(r) * nt_per_expert);
     Item it;
     it.g = __ldg(order + r);
-    it.nt = t / ntk;
-    it.kt = t - it.nt * ntk;
+    it.tm = t / tiles_n;
+    it.tn = t - it.tm * tiles_n;
     it.start = __ldg(ex + 4 * it.g + 0);
     it.len = __ldg(ex + 4 * it.g + 1);
     it.nsteps = __ldg(ex + 4 * it.g + 2);
     it.step_base = __ldg(ex + 4 * it.g + 3);
     return it;
-}
-
-// Next item of this pair's static schedule at or after pass `pass` (which is
-// advanced past it), or -1 when the schedule is exhausted.
-__device__ __forceinline__ long long item_index(long long pass, int G, int pair);
-__device__ __forceinline__ long long next_item(long long& pass, int G, int pair, long long total) {
-    while (pass * G < total) {
-        const long long i = item_index(pass, G, pair);
-        ++pass;
-        if (i < total) return i;
-    }
-    return -1;
 }
 
 // Static schedule over CTA pairs: pass p hands items [p*G, (p+1)*G) to the
@@ -343,27 +334,144 @@ __device__ __forceinline__ long long item_index(long long pass, int G, int pair)
     return pass * G + ((pass & 1) ? (G - 1 - pair) : pair);
 }
 
+// Next item of this pair's static schedule at or after pass `pass` (which is
+// advanced past it), or -1 when the schedule is exhausted.
+__device__ __forceinline__ long long next_item(long long& pass, int G, int pair, long long total) {
+    while (pass * G < total) {
+        const long long i = item_index(pass, G, pair);
+        ++pass;
+        if (i < total) return i;
+    }
+    return -1;
+}
+
+// State the MMA issuer needs besides the kernel parameters.
+struct MmaCtx {
+    uint32_t tmem, sbase, bar_empty, bar_tfull, bar_tempty, bar_drain;
+    volatile int* abort_flag;
+    int lane, G, pair;
+    long long total;
+    int nt_per_expert;
+};
+
+// MMA issuer of the leader CTA, for N-side tiles of NBLK 128-row scale blocks
+// (NBLK > 2: two MMAs per 32-token chunk, the first 256 wide). The whole warp
+// walks the schedule; one elected lane issues each tcgen05 operation. The
+// per-stage loop reads no memory and takes no data-dependent branch between
+// tcgen05 operations (the block count is a template parameter, everything
+// else sits in registers): a load, a constant-bank read of a kernel parameter
+// or an mbarrier probe here stalls the warp long enough to drain the tensor
+// pipe, so stage readiness arrives through named barriers from the watcher
+// warp. After an abort the loop still walks every stage (skipping the tensor
+// work) so that the named barriers stay paired.
+template <int NBLK>
+__device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) {
+    constexpr bool TWO = NBLK > 2;
+    constexpr uint32_t SF_COLS = 4u + 4u * NBLK;
+    constexpr uint32_t SFB_STAGE = NBLK * SF_ATOM;
+    constexpr uint32_t B2_OFF = 128u * BK;  // second MMA's rows follow the first's 128 per CTA
+    const int lane = x.lane;
+    const uint32_t tmem = x.tmem;
+    const uint32_t idesc1 = in_reg(IDESC_BASE | (static_cast<uint32_t>(p.n1 >> 3) << 17));
+    const uint32_t idesc2 = in_reg(IDESC_BASE | (static_cast<uint32_t>(p.n2 >> 3) << 17));
+    const uint32_t nstages = in_reg(static_cast<uint32_t>(p.stages));
+    const uint32_t nslots = in_reg(static_cast<uint32_t>(p.sf_slots));
+    const uint32_t sf_tmem0 = in_reg(tmem + static_cast<uint32_t>(p.tn));
+    const uint32_t a_s0 = in_reg(x.sbase);
+    const uint32_t sfa_s0 = in_reg(x.sbase + p.off_sfa);
+    const uint32_t sfb_s0 = in_reg(x.sbase + p.off_sfb);
+    const uint32_t b_s0 = in_reg(x.sbase + p.off_b);
+    const uint32_t b_stage = in_reg(p.b_stage);
+    uint32_t c = 0, tiles = 0;
+    uint32_t st = 0, slot = 0;
+    bool live = true;
+    // the next item's schedule entry is loaded one tile ahead, off the
+    // tile-boundary critical path
+    long long pass = 0;
+    long long i_next = next_item(pass, x.G, x.pair, x.total);
+    Item it_next = i_next >= 0 ? load_item(p.plan, p.E, p.tiles_n, x.nt_per_expert, i_next) : Item{};
+    while (i_next >= 0) {
+        const Item it = it_next;
+        i_next = next_item(pass, x.G, x.pair, x.total);
+        if (i_next >= 0) it_next = load_item(p.plan, p.E, p.tiles_n, x.nt_per_expert, i_next);
+        if (it.nsteps == 0) continue;
+        if (live) {
+            bool ok = true;
+            // both CTAs' epilogues have drained the accumulator; their arrivals
+            // only signal (the drained TMEM loads completed before them), so a
+            // CTA-scope acquire is enough
+            if (lane == 0)
+                ok = !*x.abort_flag && wait_phase(x.bar_tempty, (tiles & 1) ^ 1, x.abort_flag, p.wait_ns);
+            live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        tc_fence_after();
+        for (int s = 0; s < it.nsteps; ++s, ++c) {
+            named_bar_sync(BAR_READY + st, 64);
+            if (live) {
+                tc_fence_after();
+                const uint32_t sfa_t = sf_tmem0 + slot * SF_COLS;
+                const uint32_t sfb_t = sfa_t + 4;
+                const uint32_t sfa_s = sfa_s0 + st * SF_ATOM;
+                const uint32_t sfb_s = sfb_s0 + st * SFB_STAGE;
+                tc_cp_32x128b_warpx4_pair_elect(sfa_t, desc_sf_block(sfa_s));
+#pragma unroll
+                for (int b = 0; b < NBLK; ++b)
+                    tc_cp_32x128b_warpx4_pair_elect(sfb_t + 4 * b, desc_sf_block(sfb_s + b * SF_ATOM));
+                const int rem = it.len - s * BK;
+                const int nk = rem >= BK ? 4 : (rem >> 5);
+                const uint32_t a_s = a_s0 + st * A_STAGE;
+                const uint32_t b_s = b_s0 + st * b_stage;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t sel = (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
+                    const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+                    const uint64_t ad = desc_kmajor_sw128(a_s + 32 * kk);
+                    tc_mma_mxf8_pair_elect(tmem, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t, acc);
+                    if (TWO)
+                        tc_mma_mxf8_pair_elect(tmem + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk), idesc2 | sel,
+                                               sfa_t, sfb_t + 8, acc);
+                }
+                tc_commit_pair_elect(x.bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
+            }
+            named_bar_arrive(BAR_FREE + st, 64);
+            if (++st == nstages) st = 0;
+            if (++slot == nslots) slot = 0;
+        }
+        if (live) {
+            tc_commit_pair_elect(x.bar_tfull, 0x3);  // both accumulator halves complete
+            ++tiles;
+        }
+    }
+    // every MMA / copy issued for the pair has finished before teardown
+    tc_commit_pair_elect(x.bar_drain, 0x3);
+}
+
+// maps: M-side operand (boxes of 128 rows x BK tokens), N-side operand for the
+// first MMA (n1/2 rows) and for the second (n2/2 rows; unused when n2 == 0),
+// and the two sides' scale-factor blocks as u32 [blocks][128] (boxes of 1 and
+// nblk_n blocks).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
-    wgrad_main(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-               const MainParams p) {
+    wgrad_main(const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmN1,
+               const __grid_constant__ CUtensorMap tmN2, const __grid_constant__ CUtensorMap tmSFM,
+               const __grid_constant__ CUtensorMap tmSFN, const MainParams p) {
     extern __shared__ uint8_t main_smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(main_smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
     const bool leader = rank == 0;
+    const int S = p.stages;
+    const uint32_t sfb_stage = static_cast<uint32_t>(p.nblk_n) * SF_ATOM;
 
-    const uint32_t bar_full = sbase + OFF_BAR;
-    const uint32_t bar_empty = bar_full + 8 * STAGES;
-    const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+    const uint32_t bar_full = sbase + p.off_bar;
+    const uint32_t bar_empty = bar_full + 8 * S;
+    const uint32_t bar_tfull = bar_empty + 8 * S;
     const uint32_t bar_tempty = bar_tfull + 8;
     const uint32_t bar_drain = bar_tempty + 8;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_bar + 8 * (2 * S + 3));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (2 * S + 3) + 4);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);    // leader's arrive.expect_tx for both CTAs' bytes
             mbar_init(bar_empty + 8 * s, 1);   // leader's MMA commit, multicast to both CTAs
         }
@@ -372,10 +480,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         mbar_init(bar_drain, 1);               // leader's final commit, multicast
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmSFA);
-        tma_prefetch_desc(&tmSFB);
+        tma_prefetch_desc(&tmM);
+        tma_prefetch_desc(&tmN1);
+        if (p.n2) tma_prefetch_desc(&tmN2);
+        tma_prefetch_desc(&tmSFM);
+        tma_prefetch_desc(&tmSFN);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -388,114 +497,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
     // everything below reads the plan and scale blocks of the preceding kernel
     griddep_wait();
 
-    const int nt_per_expert = p.ntn2 * p.ntk;
+    const int nt_per_expert = p.tiles_m * p.tiles_n;
     const long long total = static_cast<long long>(p.E) * nt_per_expert;
     const int G = gridDim.x / 2, pair = blockIdx.x / 2;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
+            // bytes both CTAs' copies deliver to the leader's full barrier per stage
+            const uint32_t pair_tx = 2u * (static_cast<uint32_t>(A_STAGE) + p.b_stage + SF_ATOM + sfb_stage);
             const uint32_t full_leader = mapa_shared(bar_full, 0);
+            const int h1 = p.n1 >> 1, h2 = p.n2 >> 1;
             uint32_t c = 0;
+            int st = 0;
+            uint32_t ph = 0;
             bool ok = true;
             for (long long pass = 0; ok && pass * G < total; ++pass) {
                 const long long i = item_index(pass, G, pair);
                 if (i >= total) continue;
-                const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
-                const int a_row = it.nt * PAIR_M + static_cast<int>(rank) * BM;
-                const int b_row = it.kt * BN + static_cast<int>(rank) * HALF_N;
-                const int sfa_row = (it.nt * 2 + static_cast<int>(rank)) * p.ts_max + it.step_base;
-                const int sfb_row = (it.kt * p.ts_max + it.step_base) * 2;
+                const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
+                const int m_row = it.tm * PAIR_M + static_cast<int>(rank) * BM;
+                const int n_row1 = it.tn * p.tn + static_cast<int>(rank) * h1;
+                const int n_row2 = it.tn * p.tn + p.n1 + static_cast<int>(rank) * h2;
+                const int sfm_row = (it.tm * p.ts_max + it.step_base) * 2 + static_cast<int>(rank);
+                const int sfn_row = (it.tn * p.ts_max + it.step_base) * p.nblk_n;
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
-                    const int st = c % STAGES;
-                    const uint32_t ph = (c / STAGES) & 1;
                     // test hook: only the (over-declared) first fill is issued, so the
                     // stuck phase is never re-armed
                     if (p.stall_first_stage && c >= 1) { ok = false; break; }
                     if (!wait_phase(bar_empty + 8 * st, ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
                     const uint32_t fb = full_leader + 8 * st;
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * st, PAIR_TX_BYTES + (p.stall_first_stage ? 16u : 0u));
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * st, pair_tx + (p.stall_first_stage ? 16u : 0u));
                     const int x = it.start + s * BK;
-                    tma_load_2d_pair(sbase + OFF_A + st * A_STAGE, &tmA, fb, x, a_row);
-                    tma_load_2d_pair(sbase + OFF_B + st * B_STAGE, &tmB, fb, x, b_row);
-                    tma_load_2d_pair(sbase + OFF_SFA + st * SFA_STAGE, &tmSFA, fb, 0, sfa_row + s);
-                    tma_load_2d_pair(sbase + OFF_SFB + st * SFB_STAGE, &tmSFB, fb, 0, sfb_row + 2 * s);
+                    const uint32_t b_dst = sbase + p.off_b + st * p.b_stage;
+                    tma_load_2d_pair(sbase + st * A_STAGE, &tmM, fb, x, m_row);
+                    tma_load_2d_pair(b_dst, &tmN1, fb, x, n_row1);
+                    if (h2) tma_load_2d_pair(b_dst + h1 * BK, &tmN2, fb, x, n_row2);
+                    tma_load_2d_pair(sbase + p.off_sfa + st * SF_ATOM, &tmSFM, fb, 0, sfm_row + 2 * s);
+                    tma_load_2d_pair(sbase + p.off_sfb + st * sfb_stage, &tmSFN, fb, 0, sfn_row + p.nblk_n * s);
+                    if (++st == S) { st = 0; ph ^= 1; }
                 }
             }
             if (leader && (!ok || *abort_flag)) {
                 // let every copy still in flight land before the pair exits
-                const uint32_t n = c < STAGES ? c : STAGES;
+                const uint32_t n = c < static_cast<uint32_t>(S) ? c : static_cast<uint32_t>(S);
                 for (uint32_t d = 1; d <= n; ++d) {
                     const uint32_t j = c - d;
-                    drain_phase(bar_full + 8 * (j % STAGES), (j / STAGES) & 1, p.wait_ns);
+                    drain_phase(bar_full + 8 * (j % S), (j / S) & 1, p.wait_ns);
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (leader only)
-        // The whole warp walks the schedule; one elected lane issues each
-        // tcgen05 operation. The per-stage loop reads no memory: a load or an
-        // mbarrier probe here stalls this warp long enough to drain the
-        // tensor pipe, so stage readiness arrives through named barriers from
-        // the watcher warp. After an abort the loop still walks every stage
-        // (skipping the tensor work) so that the named barriers stay paired.
+        // ------------------------------------------------ MMA issuer (leader only; see mma_issue)
         if (leader) {
-            uint32_t c = 0, tiles = 0;
-            bool live = true;
-            // the next item's schedule entry is loaded one tile ahead, off the
-            // tile-boundary critical path
-            long long pass = 0;
-            long long i_next = next_item(pass, G, pair, total);
-            Item it_next = i_next >= 0 ? load_item(p.plan, p.E, p.ntk, nt_per_expert, i_next) : Item{};
-            while (i_next >= 0) {
-                const Item it = it_next;
-                i_next = next_item(pass, G, pair, total);
-                if (i_next >= 0) it_next = load_item(p.plan, p.E, p.ntk, nt_per_expert, i_next);
-                if (it.nsteps == 0) continue;
-                if (live) {
-                    bool ok = true;
-                    // both CTAs' epilogues have drained the accumulator; their arrivals
-                    // only signal (the drained TMEM loads completed before them), so a
-                    // CTA-scope acquire is enough
-                    if (lane == 0) ok = !*abort_flag && wait_phase(bar_tempty, (tiles & 1) ^ 1, abort_flag, p.wait_ns);
-                    live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                }
-                tc_fence_after();
-                for (int s = 0; s < it.nsteps; ++s, ++c) {
-                    const uint32_t st = c % STAGES;
-                    named_bar_sync(BAR_READY + st, 64);
-                    if (live) {
-                        tc_fence_after();
-                        const uint32_t sfa_t = tmem + TMEM_SFA + 4 * st;
-                        const uint32_t sfb_t = tmem + TMEM_SFB + 8 * st;
-                        const uint32_t sfa_s = sbase + OFF_SFA + st * SFA_STAGE;
-                        const uint32_t sfb_s = sbase + OFF_SFB + st * SFB_STAGE;
-                        tc_cp_32x128b_warpx4_pair_elect(sfa_t, desc_sf_block(sfa_s));
-                        tc_cp_32x128b_warpx4_pair_elect(sfb_t, desc_sf_block(sfb_s));
-                        tc_cp_32x128b_warpx4_pair_elect(sfb_t + 4, desc_sf_block(sfb_s + SF_ATOM));
-                        const int rem = it.len - s * BK;
-                        const int nk = rem >= BK ? 4 : (rem >> 5);
-                        const uint32_t a_s = sbase + OFF_A + st * A_STAGE;
-                        const uint32_t b_s = sbase + OFF_B + st * B_STAGE;
-                        for (int kk = 0; kk < nk; ++kk) {
-                            const uint32_t idesc = IDESC_BASE | (static_cast<uint32_t>(kk) << 29) |
-                                                   (static_cast<uint32_t>(kk) << 4);
-                            tc_mma_mxf8_pair_elect(tmem, desc_kmajor_sw128(a_s + 32 * kk),
-                                                   desc_kmajor_sw128(b_s + 32 * kk), idesc, sfa_t, sfb_t,
-                                                   (s > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit_pair_elect(bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
-                    }
-                    named_bar_arrive(BAR_FREE + st, 64);
-                }
-                if (live) {
-                    tc_commit_pair_elect(bar_tfull, 0x3);  // both accumulator halves complete
-                    ++tiles;
-                }
+            const MmaCtx ctx{tmem, sbase, bar_empty, bar_tfull, bar_tempty, bar_drain, abort_flag, lane, G, pair, total,
+                             nt_per_expert};
+            switch (p.nblk_n) {
+                case 1: mma_issue<1>(p, ctx); break;
+                case 2: mma_issue<2>(p, ctx); break;
+                case 3: mma_issue<3>(p, ctx); break;
+                default: mma_issue<4>(p, ctx); break;
             }
-            // every MMA / copy issued for the pair has finished before teardown
-            tc_commit_pair_elect(bar_drain, 0x3);
         }
         if (lane == 0) drain_phase(bar_drain, 0, p.wait_ns);
         __syncwarp();
@@ -503,48 +566,103 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         // ------------------------------------------------ stage watcher (leader only)
         // Waits (bounded) for each stage's data and hands it to the MMA warp
         // through BAR_READY; after an abort it stops waiting but keeps the
-        // barrier pairing until the schedule ends.
+        // barrier pairing until the schedule ends. With fewer scale-factor
+        // slots than stages it also waits until the MMAs that last read the
+        // step's slot (sf_slots steps back) have completed, before the MMA
+        // warp copies new scales into it.
         if (leader) {
             uint32_t c = 0;
             bool live = true;
+            const bool gate = p.sf_slots < S;
             for (long long pass = 0; pass * G < total; ++pass) {
                 const long long i = item_index(pass, G, pair);
                 if (i >= total) continue;
-                const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
+                const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
-                    const uint32_t st = c % STAGES;
-                    if (c >= STAGES) named_bar_sync(BAR_FREE + st, 64);  // MMA warp took the previous fill
+                    const uint32_t st = c % S;
+                    if (c >= static_cast<uint32_t>(S)) named_bar_sync(BAR_FREE + st, 64);  // MMA warp took the previous fill
                     if (live) {
                         bool ok = true;
-                        if (lane == 0) ok = wait_phase(bar_full + 8 * st, (c / STAGES) & 1, abort_flag, p.wait_ns);
+                        if (lane == 0) {
+                            ok = wait_phase(bar_full + 8 * st, (c / S) & 1, abort_flag, p.wait_ns);
+                            if (ok && gate && c >= static_cast<uint32_t>(p.sf_slots)) {
+                                const uint32_t j = c - p.sf_slots;
+                                ok = wait_phase(bar_empty + 8 * (j % S), (j / S) & 1, abort_flag, p.wait_ns);
+                            }
+                        }
                         live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     }
                     named_bar_arrive(BAR_READY + st, 64);
                 }
             }
             // consume the MMA warp's last BAR_FREE arrivals so every id ends paired
-            for (uint32_t d = c < STAGES ? c : STAGES; d > 0; --d) named_bar_sync(BAR_FREE + (c - d) % STAGES, 64);
+            for (uint32_t d = c < static_cast<uint32_t>(S) ? c : static_cast<uint32_t>(S); d > 0; --d)
+                named_bar_sync(BAR_FREE + (c - d) % S, 64);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (8 warps per CTA)
-        const int q = warp & 3;          // TMEM lane quarter this warp may access
-        const int h = (warp - 3) >> 2;   // column half of the 256-wide tile
+        // TMEM lane = M-side row of this CTA's half, column = N-side row of the
+        // tile. Two warps share each 32-lane quarter, each draining half of the
+        // tn columns (at most 224) in 32-column loads: up to four chunks in
+        // flight at once; with more than four, the first four are stored
+        // before the rest is loaded (registers hold 128 columns at most). The
+        // accumulator is released after the last load.
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int h = (warp - EPI_WARP0) >> 2;  // column half of the tile
+        const int ncols = p.tn >> 1;
+        const int nchunks = (ncols + 31) >> 5;
         const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
+        const bool odd = lane & 1;
         uint32_t tiles = 0;
         for (long long pass = 0; pass * G < total; ++pass) {
             const long long i = item_index(pass, G, pair);
             if (i >= total) continue;
-            const Item it = load_item(p.plan, p.E, p.ntk, nt_per_expert, i);
-            const int row = it.nt * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;
-            const int col0 = it.kt * BN + h * 128;
-            uint16_t* orow = p.out + (static_cast<size_t>(it.g) * p.N + row) * static_cast<size_t>(p.K) + col0;
-            if (it.nsteps == 0) {
-                // expert without tokens: exact +0.0 slab
-                if (row < p.N) {
-                    for (int c = 0; c < 128; c += 8)
-                        if (col0 + c < p.K) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+            const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
+            const int mrow = it.tm * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;  // this lane's M-side row
+            const int ncol0 = it.tn * p.tn + h * ncols;                                      // first N-side row here
+            // NK: a lane owns output row mrow; KN: a lane owns output column
+            // mrow, and lane pairs share the column pair (k2, k2 + 1)
+            const int k2 = mrow & ~1;
+            const bool row_in = p.kn ? (k2 < p.K) : (mrow < p.N);
+            uint16_t* obase = p.kn ? p.out + static_cast<size_t>(it.g) * p.N * static_cast<size_t>(p.K) + k2
+                                   : p.out + (static_cast<size_t>(it.g) * p.N + mrow) * static_cast<size_t>(p.K) + ncol0;
+            // Narrow one 32-column chunk (columns 32 j .. 32 j + 31 of this warp's
+            // half) to bf16 and store it. NK: 16-byte runs of the lane's row.
+            // KN: neighbouring lanes swap their (n, n+1) pairs so that the even
+            // lane stores (k, k+1) of row n and the odd lane (k, k+1) of row
+            // n+1: 4-byte stores, 64 contiguous bytes per row and instruction.
+            auto store_chunk = [&](int j, const uint32_t (&v)[32]) {
+                if (!p.kn) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        const int cc = 32 * j + c;
+                        if (row_in && cc < ncols && ncol0 + cc < p.K)
+                            *reinterpret_cast<uint4*>(obase + cc) =
+                                make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
+                                           pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const int cc = 32 * j + c;
+                        if (cc < ncols) {  // the same for the whole warp
+                            const uint32_t mine = pack_bf16x2(v[c], v[c + 1]);
+                            const uint32_t got = __shfl_xor_sync(0xffffffffu, mine, 1);
+                            // even: (own n, partner n) = row n; odd: (partner n+1, own n+1) = row n+1
+                            const uint32_t w = odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
+                            const int n = ncol0 + cc + (odd ? 1 : 0);
+                            if (row_in && n < p.N) *reinterpret_cast<uint32_t*>(obase + static_cast<size_t>(n) * p.K) = w;
+                        }
+                    }
                 }
+            };
+            if (it.nsteps == 0) {
+                // expert without tokens: an exact +0.0 tile, no accumulator involved
+                uint32_t z[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) z[c] = 0u;
+                for (int j = 0; j < nchunks; ++j) store_chunk(j, z);
                 continue;
             }
             // one lane waits, the warp follows its verdict (the TMEM loads below
@@ -553,37 +671,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             if (lane == 0) ready = wait_phase(bar_tfull, tiles & 1, abort_flag, p.wait_ns);
             if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
             tc_fence_after();
-            uint32_t v[4][32];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 128);
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * ncols);
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    // this CTA's accumulator half may be overwritten
+                    if (leader) mbar_arrive(bar_tempty);
+                    else mbar_arrive_cluster(tempty_leader);
+                }
+            };
+#pragma unroll 1
+            for (int j0 = 0; j0 < nchunks; j0 += 4) {
+                uint32_t v[4][32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32 * j, v[j]);
-            tmem_wait_ld();
+                for (int j = 0; j < 4; ++j)
+                    if (j0 + j < nchunks) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
+                tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                // this CTA's accumulator half may be overwritten
-                if (leader) mbar_arrive(bar_tempty);
-                else mbar_arrive_cluster(tempty_leader);
+                for (int j = 0; j < 4; ++j) reg_fence(v[j]);
+                if (j0 + 4 >= nchunks) release();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (j0 + j < nchunks) store_chunk(j0 + j, v[j]);
             }
             ++tiles;
-            if (row < p.N) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        if (col0 + 32 * j + c < p.K) {
-                            uint4 o;
-                            o.x = pack_bf16x2(v[j][c + 0], v[j][c + 1]);
-                            o.y = pack_bf16x2(v[j][c + 2], v[j][c + 3]);
-                            o.z = pack_bf16x2(v[j][c + 4], v[j][c + 5]);
-                            o.w = pack_bf16x2(v[j][c + 6], v[j][c + 7]);
-                            *reinterpret_cast<uint4*>(orow + 32 * j + c) = o;
-                        }
-                    }
-                }
-            }
         }
     }
 
@@ -597,56 +709,187 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
 
 // ============================================================== host side
 
-bool ws_layout(int E, int N, int K, int64_t M, WsLayout* L) {
+namespace {
+
+// Shared-memory and TMEM geometry of the main kernel for an N-side tile of
+// tn rows; false if it does not fit.
+struct Geometry {
+    int stages, sf_slots;
+    uint32_t off_b, off_sfa, off_sfb, off_bar, b_stage, smem_bytes;
+};
+
+bool geometry(int tn, Geometry* g) {
+    const int nblk = (tn + 127) / 128;
+    const uint32_t b_stage = static_cast<uint32_t>(tn / 2) * BK;  // multiple of 1024 (tn % 16 == 0)
+    const uint32_t per_stage = A_STAGE + b_stage + SF_ATOM + nblk * SF_ATOM + 16;  // + two mbarriers
+    const uint32_t fixed = 1024 + 3 * 8 + 16;  // alignment slack, tile barriers, abort flag / TMEM slot
+    int stages = static_cast<int>((MAIN_SMEM_MAX - fixed) / per_stage);
+    if (stages > MAX_STAGES) stages = MAX_STAGES;
+    const int sf_cols = 4 + 4 * nblk;
+    int slots = (static_cast<int>(TMEM_COLS) - tn) / sf_cols;
+    if (slots > stages) slots = stages;
+    if (stages < 3 || slots < 2) return false;
+    g->stages = stages;
+    g->sf_slots = slots;
+    g->b_stage = b_stage;
+    g->off_b = static_cast<uint32_t>(stages) * A_STAGE;
+    g->off_sfa = g->off_b + stages * b_stage;
+    g->off_sfb = g->off_sfa + stages * SF_ATOM;
+    g->off_bar = g->off_sfb + stages * nblk * SF_ATOM;
+    g->smem_bytes = g->off_bar + 8 * (2 * stages + 3) + 16 + 1024;
+    return g->smem_bytes <= static_cast<uint32_t>(MAIN_SMEM_MAX);
+}
+
+// Relative time per computed output column of one pair K-step with an
+// N-side tile of tn rows, measured with this kernel on GB300 under its power
+// cap (whole-kernel time / (tiles x tn), normalised to tn = 256, on the 671B
+// up/gate and down expert shapes with the 256 side on A). Narrow tiles pay the
+// per-step scale-factor copies and the M-side operand bytes over fewer
+// columns; tn just above 256 adds a second MMA too narrow to run at full
+// rate; around 384-448 the operand bytes per column are lowest.
+double column_cost(int tn) {
+    static const double f[] = {
+        // tn = 16, 32, ..., 448
+        3.00, 2.60, 2.30, 2.00, 1.85, 1.70, 1.60, 1.49,          // 16 .. 128
+        1.28, 1.175, 1.14, 1.063, 1.063, 1.002, 0.985, 1.00,     // 144 .. 256
+        1.094, 1.039, 1.066, 1.023, 0.982, 0.979, 0.948, 0.914,  // 272 .. 384
+        0.919, 0.89, 0.912, 0.902};                             // 400 .. 448
+    return f[tn / 16 - 1];
+}
+
+TileConfig make_config(int kn, int tn, int rows_m, int rows_n) {
+    TileConfig tc;
+    tc.kn = kn;
+    tc.tn = tn;
+    tc.n1 = tn < 256 ? tn : 256;
+    tc.n2 = tn - tc.n1;
+    tc.nblk_n = (tn + 127) / 128;
+    tc.tiles_m = (rows_m + PAIR_M - 1) / PAIR_M;
+    tc.tiles_n = (rows_n + tn - 1) / tn;
+    return tc;
+}
+
+// Best tile of one orientation: the modelled time of all tiles of an expert
+// of `steps` K-steps over every admissible tn; ties keep the larger tn. The
+// measured column costs include the tile hand-overs at 65-130 K-steps per
+// tile; a tile wider than 256 hands over more slowly (its epilogue stores
+// half of its columns before loading the rest), worth about three more
+// K-steps. The 256 side on B measured about 5% slower (4-byte pair stores).
+TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, double* cost) {
+    TileConfig best{};
+    double best_cost = -1.0;
+    for (int tn = MAX_TN; tn >= 16; tn -= 16) {
+        if (force_tn && tn != force_tn) continue;
+        Geometry g;
+        if (!geometry(tn, &g)) continue;
+        const TileConfig tc = make_config(kn, tn, rows_m, rows_n);
+        const double epi = kn ? 1.05 : 1.0;
+        const double c = static_cast<double>(tc.tiles_m) * tc.tiles_n * tn * column_cost(tn) * epi *
+                         (steps + (tn > 256 ? 3.0 : 0.0));
+        if (best_cost < 0 || c < best_cost * (1.0 - 1e-9)) {
+            best_cost = c;
+            best = tc;
+        }
+    }
+    *cost = best_cost;
+    return best;
+}
+
+}  // namespace
+
+bool choose_tiles(int N, int K, int E, int64_t M, int force, int force_tn, TileConfig* tc) {
+    if (N < 1 || K < 1) return false;
+    if (force_tn && (force_tn < 16 || force_tn > MAX_TN || force_tn % 16)) return false;
+    const double steps = (E > 0 && M > 0) ? static_cast<double>(M) / (static_cast<double>(E) * BK) + 1.0 : 32.0;
+    double c_nk, c_kn;
+    const TileConfig nk = best_of(0, N, K, steps, force_tn, &c_nk);
+    const TileConfig kn = best_of(1, K, N, steps, force_tn, &c_kn);
+    if (c_nk < 0 || c_kn < 0) return false;
+    if (force == 1) *tc = nk;
+    else if (force == 2) *tc = kn;
+    else *tc = c_kn < c_nk * (1.0 - 1e-9) ? kn : nk;  // ties keep the row-contiguous epilogue
+    return true;
+}
+
+bool ws_layout(int E, int N, int K, int64_t M, const TileConfig& tc, WsLayout* L) {
     if (E < 1 || E > MXFP8_MAX_EXPERTS || N < 1 || K < 1 || M < 32 || (M % 32) != 0) return false;
     if (M > (int64_t(1) << 31) - 256) return false;
-    L->ntn = (N + BM - 1) / BM;
-    L->ntk = (K + BN - 1) / BN;
     const int64_t ts = (M + BK - 1) / BK + E;
-    if (ts > (int64_t(1) << 30)) return false;
+    // scale-factor block rows (tile * ts_max + step) * blocks + block are int32 TMA coordinates
+    const int64_t rows_m = static_cast<int64_t>(tc.tiles_m) * ts * 2;
+    const int64_t rows_n = static_cast<int64_t>(tc.tiles_n) * ts * tc.nblk_n;
+    if (rows_m > (int64_t(1) << 31) - 1 || rows_n > (int64_t(1) << 31) - 1) return false;
     L->ts_max = static_cast<int>(ts);
+    L->tc = tc;
     const size_t plan_bytes = sizeof(int32_t) * (PLAN_HDR + 5 * static_cast<size_t>(E));
     L->plan_off = 0;
-    L->sfa_off = (plan_bytes + 1023) & ~size_t(1023);
-    L->sfb_off = L->sfa_off + static_cast<size_t>(L->ntn) * L->ts_max * SF_ATOM;
-    L->total = L->sfb_off + static_cast<size_t>(L->ntk) * L->ts_max * 2 * SF_ATOM;
+    L->sfm_off = (plan_bytes + 1023) & ~size_t(1023);
+    L->sfn_off = L->sfm_off + static_cast<size_t>(rows_m) * SF_ATOM;
+    L->total = L->sfn_off + static_cast<size_t>(rows_n) * SF_ATOM;
     return true;
+}
+
+size_t ws_bytes_any_orientation(int E, int N, int K, int64_t M, int force_tn) {
+    size_t most = 0;
+    for (int force = 1; force <= 2; ++force) {
+        TileConfig tc;
+        WsLayout L;
+        if (!choose_tiles(N, K, E, M, force, force_tn, &tc) || !ws_layout(E, N, K, M, tc, &L)) return 0;
+        if (L.total > most) most = L.total;
+    }
+    return most;
 }
 
 cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what) {
     const WsLayout& L = a.lay;
+    const TileConfig& tc = L.tc;
     int32_t* plan = reinterpret_cast<int32_t*>(a.ws + L.plan_off);
-    uint8_t* sfa = a.ws + L.sfa_off;
-    uint8_t* sfb = a.ws + L.sfb_off;
+    Geometry geo;
+    *what = "tile geometry";
+    if (!geometry(tc.tn, &geo)) return cudaErrorInvalidConfiguration;
 
     *what = "plan / scale re-layout kernel";
     {
+        PrepSide sm_side, sn_side;
+        sm_side.plane = tc.kn ? a.sB : a.sA;
+        sm_side.rows = tc.kn ? a.K : a.N;
+        sm_side.tile_rows = PAIR_M;
+        sm_side.tiles = tc.tiles_m;
+        sm_side.blocks = 2;
+        sm_side.sf = a.ws + L.sfm_off;
+        sn_side.plane = tc.kn ? a.sA : a.sB;
+        sn_side.rows = tc.kn ? a.N : a.K;
+        sn_side.tile_rows = tc.tn;
+        sn_side.tiles = tc.tiles_n;
+        sn_side.blocks = tc.nblk_n;
+        sn_side.sf = a.ws + L.sfn_off;
         // enough blocks for every task of the largest possible plan, at most 4 per SM
-        const long long tasks = static_cast<long long>(L.ntn + 2 * L.ntk) *
+        const long long tasks = (2LL * tc.tiles_m + static_cast<long long>(tc.nblk_n) * tc.tiles_n) *
                                 ((L.ts_max + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS);
         long long blocks = tasks;
         if (blocks > 4LL * a.num_sms) blocks = 4LL * a.num_sms;
         if (blocks < 1) blocks = 1;
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
                           sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
-        wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(
-            a.offs, a.sA, a.sB, plan, sfa, sfb, a.E, a.N, a.K, a.M, L.ts_max, L.ntn, L.ntk);
+        wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(a.offs, sm_side, sn_side, plan, a.E,
+                                                                                    a.M, L.ts_max);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
 
     *what = "main contraction kernel";
     // per device: the shared-memory opt-in and the number of CTA pairs that
-    // can be resident at once (the persistent grid)
+    // can be resident at once (the persistent grid; one CTA per SM whatever
+    // the tile, as the register file holds only one)
     static int max_pairs[64] = {};
     if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
     if (max_pairs[a.dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(wgrad_main, cudaFuncAttributeMaxDynamicSharedMemorySize, MAIN_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(wgrad_main, cudaFuncAttributeMaxDynamicSharedMemorySize, MAIN_SMEM_MAX);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(2 * (a.num_sms / 2));
         q.blockDim = dim3(MAIN_THREADS);
-        q.dynamicSmemBytes = MAIN_SMEM;
+        q.dynamicSmemBytes = MAIN_SMEM_MAX;
         int clusters = 0;
         e = cudaOccupancyMaxActiveClusters(&clusters, wgrad_main, &q);
         if (e != cudaSuccess) return e;
@@ -660,30 +903,42 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     mp.N = a.N;
     mp.K = a.K;
     mp.ts_max = L.ts_max;
-    mp.ntn2 = (a.N + PAIR_M - 1) / PAIR_M;
-    mp.ntk = L.ntk;
+    mp.tiles_m = tc.tiles_m;
+    mp.tiles_n = tc.tiles_n;
+    mp.tn = tc.tn;
+    mp.n1 = tc.n1;
+    mp.n2 = tc.n2;
+    mp.nblk_n = tc.nblk_n;
+    mp.kn = tc.kn;
+    mp.stages = geo.stages;
+    mp.sf_slots = geo.sf_slots;
+    mp.off_b = geo.off_b;
+    mp.off_sfa = geo.off_sfa;
+    mp.off_sfb = geo.off_sfb;
+    mp.off_bar = geo.off_bar;
+    mp.b_stage = geo.b_stage;
     mp.wait_ns = a.wait_limit_ns;
     mp.stall_first_stage = a.stall_first_stage;
-    const long long total = static_cast<long long>(a.E) * mp.ntn2 * mp.ntk;
+    const long long total = static_cast<long long>(a.E) * tc.tiles_m * tc.tiles_n;
     const int pairs = static_cast<int>(total < max_pairs[a.dev] ? total : max_pairs[a.dev]);
     if (a.ev_before) {
         cudaError_t e = cudaEventRecord(a.ev_before, a.stream);
         if (e != cudaSuccess) return e;
     }
     // programmatic dependent launch: the prologue (barriers, TMEM allocation,
-    // descriptor prefetch) overlaps the prep kernel; griddepcontrol.wait in
-    // the kernel orders every read of the prep kernel's output after it
+    // descriptor prefetch) overlaps the prep kernel's tail; griddepcontrol.wait
+    // in the kernel orders every read of the prep kernel's output after it
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(MAIN_THREADS);
-    cfg.dynamicSmemBytes = MAIN_SMEM;
+    cfg.dynamicSmemBytes = geo.smem_bytes;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], mp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], maps[4], mp);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

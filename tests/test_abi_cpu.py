@@ -98,3 +98,80 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(ImportError):
         _lib.load()
+
+
+def test_tile_config_choice(lib):
+    """Host-side tiling: the automatic mode follows the kernel's cost model
+    (bytes per step against MMA cycles, padding, tile count); either
+    orientation and any admissible tile width can be forced; invalid settings
+    fail."""
+    try:
+        mx.set_tile_orientation(0)
+        mx.set_tile_rows(0)
+        # 16B expert shape: N = 1408 is 5.5 x 256 but 6 x 240 (2% padding) -> 256 side on B
+        assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 1, "tn": 240, "tiles_m": 8, "tiles_n": 6}
+        # 671B up/gate: K = 7168 = 16 x 448 with the 256 side on A (N = 4096)
+        assert mx.tile_config(32, 4096, 7168, 262144) == {"kn": 0, "tn": 448, "tiles_m": 16, "tiles_n": 16}
+        # 671B down: K = 2048 in 5 tiles of 416 (1.6% padding), the 256 side on A (N = 7168)
+        assert mx.tile_config(32, 7168, 2048, 524288) == {"kn": 0, "tn": 416, "tiles_m": 28, "tiles_n": 5}
+        mx.set_tile_orientation(1)
+        assert mx.tile_config(8, 1408, 2048, 32768)["kn"] == 0
+        mx.set_tile_rows(256)
+        assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 0, "tn": 256, "tiles_m": 6, "tiles_n": 8}
+        mx.set_tile_orientation(2)
+        mx.set_tile_rows(176)
+        assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 1, "tn": 176, "tiles_m": 8, "tiles_n": 8}
+        for bad in (3, -1):
+            with pytest.raises(mx.Mxfp8Error):
+                mx.set_tile_orientation(bad)
+        for bad in (8, 24, 464, -16):
+            with pytest.raises(mx.Mxfp8Error):
+                mx.set_tile_rows(bad)
+        with pytest.raises(mx.Mxfp8Error):
+            mx.tile_config(4, 0, 8, 1024)
+    finally:
+        mx.set_tile_orientation(0)
+        mx.set_tile_rows(0)
+
+
+def test_tile_config_covers_output(lib):
+    """Whatever the model picks, tn is a multiple of 16 in [16, 448] and the
+    tiles cover both output axes."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    try:
+        for mode in (0, 1, 2):
+            mx.set_tile_orientation(mode)
+            for _ in range(40):
+                N = int(rng.integers(1, 9000))
+                K = 8 * int(rng.integers(1, 1200))
+                E = int(rng.integers(1, 300))
+                M = 32 * int(rng.integers(1, 20000))
+                cfg = mx.tile_config(E, N, K, M)
+                tn = cfg["tn"]
+                assert tn % 16 == 0 and 16 <= tn <= 448
+                if mode:
+                    assert cfg["kn"] == mode - 1
+                rows_m, rows_n = (K, N) if cfg["kn"] else (N, K)
+                assert cfg["tiles_m"] == -(-rows_m // 256)
+                assert cfg["tiles_n"] == -(-rows_n // tn)
+    finally:
+        mx.set_tile_orientation(0)
+
+
+def test_workspace_covers_both_orientations(lib):
+    """The workspace size is the larger of the two orientations' needs: the
+    plan, then 2 scale blocks per 256-row tile and ceil(tn/128) per tn-row tile,
+    each for the K-step bound ceil(M/128) + E."""
+    E, N, K, M = 8, 1408, 2048, 196608
+    ts = -(-M // 128) + E
+    plan = -(-4 * (8 + 5 * E) // 1024) * 1024
+    need = []
+    try:
+        for mode in (1, 2):
+            mx.set_tile_orientation(mode)
+            c = mx.tile_config(E, N, K, M)
+            need.append(plan + (c["tiles_m"] * 2 + c["tiles_n"] * -(-c["tn"] // 128)) * ts * 512)
+    finally:
+        mx.set_tile_orientation(0)
+    assert lib.mxfp8_wgrad_workspace_bytes(E, N, K, M) == max(need)

@@ -247,3 +247,62 @@ def test_invalid_offsets_are_clamped_and_flagged():
     clamped = np.array([288, 288, 1024, 1024], np.int32)
     check_tol(got, A, sA, B, sB, clamped, E, N, K, M)
     assert mx.device_status(clear=True) == 0
+
+
+# ------------------------------------------------------------------ tilings
+
+@pytest.fixture
+def tiling_reset():
+    yield
+    mx.set_tile_orientation(0)
+    mx.set_tile_rows(0)
+
+
+# (orientation mode, forced tile rows): the model's choice per orientation,
+# one-MMA tiles, two-MMA tiles (the second 16 columns wide, or 192), narrow tiles
+TILINGS = [(1, 0), (2, 0), (1, 256), (2, 448), (1, 272), (2, 160), (1, 48)]
+
+
+@pytest.mark.parametrize("E,N,K,M,sizes", [
+    (4, 1408, 1152, 2048, [800, 352, 0, 896]),        # N, K not multiples of any tile
+    (3, 320, 640, 1536, [608, 0, 928]),               # ragged on both sides
+    (1, 40, 8, 512, [512]),                           # tiles far larger than the output
+    (2, 136, 264, 1024, [544, 480]),                  # odd tile counts
+    (2, 1408, 2048, 2048, [1120, 928]),               # the 16B expert shape
+])
+def test_tilings_bit_identical(E, N, K, M, sizes, tiling_reset):
+    """Every tiling accumulates each output element from the same 32-token
+    block products in the same order, so all of them must agree bit for bit,
+    and match the oracle."""
+    A, sA = quantised_operand(N, M, seed=E * 7 + N, stream=0)
+    B, sB = quantised_operand(K, M, seed=E * 7 + N, stream=1)
+    offs = np.cumsum(sizes).astype(np.int32)
+    outs = []
+    for mode, tn in TILINGS:
+        mx.set_tile_orientation(mode)
+        mx.set_tile_rows(tn)
+        cfg = mx.tile_config(E, N, K, M)
+        assert cfg["kn"] == mode - 1 and (tn == 0 or cfg["tn"] == tn)
+        outs.append(run_gpu(A, sA, B, sB, offs, E, N, K))
+    for (mode, tn), o in zip(TILINGS[1:], outs[1:]):
+        assert np.array_equal(outs[0], o), f"tiling mode={mode} tn={tn} differs"
+    check_tol(outs[0], A, sA, B, sB, offs, E, N, K, M)
+
+
+def test_tilings_exact_integers(tiling_reset):
+    """Integer-valued operands whose sums are exact in fp32: every tiling
+    rounds the exact sum to bf16 and gives the oracle's bits exactly."""
+    rng = np.random.default_rng(71)
+    E, N, K, M = 3, 200, 344, 1536
+    vals = np.array([0x38, 0x40, 0xB8, 0xC0, 0x00], np.uint8)  # +-1, +-2, 0 in E4M3
+    A = vals[rng.integers(0, 5, (N, M))]
+    B = vals[rng.integers(0, 5, (K, M))]
+    sA = np.full((N, M // 32), 127, np.uint8)
+    sB = np.full((K, M // 32), 127, np.uint8)
+    offs = np.array([224, 224, 1536], np.int32)
+    ref = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M)
+    for mode, tn in TILINGS:
+        mx.set_tile_orientation(mode)
+        mx.set_tile_rows(tn)
+        got = run_gpu(A, sA, B, sB, offs, E, N, K)
+        assert same_bits_signless_zero(got, ref), f"tiling mode={mode} tn={tn}"
