@@ -182,16 +182,26 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
             const long long left = (static_cast<long long>(s_end[lo]) - t0 + 31) >> 5;
             nvalid = static_cast<int>(left < 4 ? left : 4);
         }
-        for (int r = warp; r < PREP_ROWS; r += PREP_THREADS / 32) {
-            const int row = row0 + r;
-            uint32_t wv = 0;
-            if (in_tile0 + r < sd.tile_rows && row < sd.rows) {
-                const uint8_t* src = sd.plane + static_cast<size_t>(row) * sM + col;
+        // all of this warp's rows are loaded before any is stored, so the
+        // loads of a task are in flight together (one memory latency, not 16)
+        constexpr int ROWS_PER_WARP = PREP_ROWS / (PREP_THREADS / 32);
+        uint8_t bv[ROWS_PER_WARP][4];
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    if (kb < nvalid) wv |= static_cast<uint32_t>(__ldg(src + kb)) << (8 * kb);
-            }
-            tile[r * (PREP_TILE_STEPS + 1) + lane] = wv;
+        for (int i = 0; i < ROWS_PER_WARP; ++i) {
+            const int r = warp + i * (PREP_THREADS / 32);
+            const int row = row0 + r;
+            const bool ok = in_tile0 + r < sd.tile_rows && row < sd.rows;
+            const uint8_t* src = sd.plane + static_cast<size_t>(ok ? row : 0) * sM + col;
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) bv[i][kb] = (ok && kb < nvalid) ? __ldg(src + kb) : uint8_t(0);
+        }
+#pragma unroll
+        for (int i = 0; i < ROWS_PER_WARP; ++i) {
+            const int r = warp + i * (PREP_THREADS / 32);
+            tile[r * (PREP_TILE_STEPS + 1) + lane] = static_cast<uint32_t>(bv[i][0]) |
+                                                     (static_cast<uint32_t>(bv[i][1]) << 8) |
+                                                     (static_cast<uint32_t>(bv[i][2]) << 16) |
+                                                     (static_cast<uint32_t>(bv[i][3]) << 24);
         }
         __syncthreads();
         // block j of this task: lane r0 writes rows r0, r0+32, r0+64, r0+96 (16 bytes)
@@ -863,17 +873,22 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         sn_side.tiles = tc.tiles_n;
         sn_side.blocks = tc.nblk_n;
         sn_side.sf = a.ws + L.sfn_off;
-        // enough blocks for every task of the largest possible plan, at most 4 per SM
+        // enough blocks for every task of the largest possible plan, at most as
+        // many as are resident at once (one wave)
         const long long tasks = (2LL * tc.tiles_m + static_cast<long long>(tc.nblk_n) * tc.tiles_n) *
                                 ((L.ts_max + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS);
-        long long blocks = tasks;
-        if (blocks > 4LL * a.num_sms) blocks = 4LL * a.num_sms;
-        if (blocks < 1) blocks = 1;
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
                           sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wgrad_prep, PREP_THREADS, sm);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+        long long blocks = tasks;
+        if (blocks > static_cast<long long>(per_sm) * a.num_sms) blocks = static_cast<long long>(per_sm) * a.num_sms;
+        if (blocks < 1) blocks = 1;
         wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(a.offs, sm_side, sn_side, plan, a.E,
                                                                                     a.M, L.ts_max);
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
 
