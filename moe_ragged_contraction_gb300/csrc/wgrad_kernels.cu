@@ -36,6 +36,8 @@
 // partial step; the last step of a group issues only the ceil(rem/32) MMAs
 // that cover its tokens, so bytes past the group end (the next expert's, or
 // padding that may hold NaN) are loaded but never consumed.
+#include <type_traits>
+
 #include "mxw_internal.h"
 #include "mxw_ptx.cuh"
 #include "../../include/mxfp8_wgrad.h"
@@ -276,6 +278,9 @@ struct MainParams {
     int nblk_n;              // 128-row scale blocks per N-side tile
     int kn;                  // 0: M side = rows of A (n), N side = rows of B (k); 1: swapped
     int stages, sf_slots;
+    int acc_bufs;            // accumulators in TMEM (2: the next tile's MMAs overlap this tile's drain)
+    int wide_stores;         // 32-byte output stores (rows of 16 columns 32-byte aligned), else 16-byte
+    uint32_t sf_col0;        // first TMEM column of the scale-factor slots
     uint32_t off_b, off_sfa, off_sfb, off_bar, b_stage;  // shared-memory layout (bytes)
     unsigned long long wait_ns;
     int stall_first_stage;   // test hook: over-declare the first stage's bytes so its wait runs out
@@ -355,9 +360,33 @@ __device__ __forceinline__ long long next_item(long long& pass, int G, int pair,
     return -1;
 }
 
+// This pair's items in schedule order, the next item's plan entry loaded one
+// item ahead so that its global-memory latency overlaps the current item.
+struct ItemStream {
+    const int32_t* plan;
+    int E, tiles_n, nt_per_expert, G, pair;
+    long long total, pass, i_next;
+    Item it_next;
+
+    __device__ __forceinline__ ItemStream(const int32_t* plan_, int E_, int tiles_n_, int ntpe, int G_, int pair_,
+                                          long long total_)
+        : plan(plan_), E(E_), tiles_n(tiles_n_), nt_per_expert(ntpe), G(G_), pair(pair_), total(total_), pass(0) {
+        i_next = next_item(pass, G, pair, total);
+        if (i_next >= 0) it_next = load_item(plan, E, tiles_n, nt_per_expert, i_next);
+    }
+
+    __device__ __forceinline__ bool next(Item& it) {
+        if (i_next < 0) return false;
+        it = it_next;
+        i_next = next_item(pass, G, pair, total);
+        if (i_next >= 0) it_next = load_item(plan, E, tiles_n, nt_per_expert, i_next);
+        return true;
+    }
+};
+
 // State the MMA issuer needs besides the kernel parameters.
 struct MmaCtx {
-    uint32_t tmem, sbase, bar_empty, bar_tfull, bar_tempty, bar_drain;
+    uint32_t tmem, sbase, bar_empty, bar_tfull, bar_tempty, bar_drain;  // tfull / tempty: one per accumulator
     volatile int* abort_flag;
     int lane, G, pair;
     long long total;
@@ -386,24 +415,20 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
     const uint32_t idesc2 = in_reg(IDESC_BASE | (static_cast<uint32_t>(p.n2 >> 3) << 17));
     const uint32_t nstages = in_reg(static_cast<uint32_t>(p.stages));
     const uint32_t nslots = in_reg(static_cast<uint32_t>(p.sf_slots));
-    const uint32_t sf_tmem0 = in_reg(tmem + static_cast<uint32_t>(p.tn));
+    const uint32_t sf_tmem0 = in_reg(tmem + p.sf_col0);
+    const uint32_t nbuf = in_reg(static_cast<uint32_t>(p.acc_bufs));
+    const uint32_t acc_cols = in_reg(static_cast<uint32_t>(p.tn));
     const uint32_t a_s0 = in_reg(x.sbase);
     const uint32_t sfa_s0 = in_reg(x.sbase + p.off_sfa);
     const uint32_t sfb_s0 = in_reg(x.sbase + p.off_sfb);
     const uint32_t b_s0 = in_reg(x.sbase + p.off_b);
     const uint32_t b_stage = in_reg(p.b_stage);
-    uint32_t c = 0, tiles = 0;
-    uint32_t st = 0, slot = 0;
+    uint32_t c = 0;
+    uint32_t st = 0, slot = 0, buf = 0, acc_phase = 0;  // accumulator buffer of the current tile and its use count parity
     bool live = true;
-    // the next item's schedule entry is loaded one tile ahead, off the
-    // tile-boundary critical path
-    long long pass = 0;
-    long long i_next = next_item(pass, x.G, x.pair, x.total);
-    Item it_next = i_next >= 0 ? load_item(p.plan, p.E, p.tiles_n, x.nt_per_expert, i_next) : Item{};
-    while (i_next >= 0) {
-        const Item it = it_next;
-        i_next = next_item(pass, x.G, x.pair, x.total);
-        if (i_next >= 0) it_next = load_item(p.plan, p.E, p.tiles_n, x.nt_per_expert, i_next);
+    ItemStream items(p.plan, p.E, p.tiles_n, x.nt_per_expert, x.G, x.pair, x.total);
+    Item it;
+    while (items.next(it)) {
         if (it.nsteps == 0) continue;
         if (live) {
             bool ok = true;
@@ -411,10 +436,11 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
             // only signal (the drained TMEM loads completed before them), so a
             // CTA-scope acquire is enough
             if (lane == 0)
-                ok = !*x.abort_flag && wait_phase(x.bar_tempty, (tiles & 1) ^ 1, x.abort_flag, p.wait_ns);
+                ok = !*x.abort_flag && wait_phase(x.bar_tempty + 8 * buf, acc_phase ^ 1, x.abort_flag, p.wait_ns);
             live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
         tc_fence_after();
+        const uint32_t acc_t = tmem + buf * acc_cols;
         for (int s = 0; s < it.nsteps; ++s, ++c) {
             named_bar_sync(BAR_READY + st, 64);
             if (live) {
@@ -435,9 +461,9 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
                     const uint32_t sel = (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
                     const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t ad = desc_kmajor_sw128(a_s + 32 * kk);
-                    tc_mma_mxf8_pair_elect(tmem, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t, acc);
+                    tc_mma_mxf8_pair_elect(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t, acc);
                     if (TWO)
-                        tc_mma_mxf8_pair_elect(tmem + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk), idesc2 | sel,
+                        tc_mma_mxf8_pair_elect(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk), idesc2 | sel,
                                                sfa_t, sfb_t + 8, acc);
                 }
                 tc_commit_pair_elect(x.bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
@@ -447,8 +473,11 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
             if (++slot == nslots) slot = 0;
         }
         if (live) {
-            tc_commit_pair_elect(x.bar_tfull, 0x3);  // both accumulator halves complete
-            ++tiles;
+            tc_commit_pair_elect(x.bar_tfull + 8 * buf, 0x3);  // both accumulator halves complete
+            if (++buf == nbuf) {
+                buf = 0;
+                acc_phase ^= 1;
+            }
         }
     }
     // every MMA / copy issued for the pair has finished before teardown
@@ -474,19 +503,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
 
     const uint32_t bar_full = sbase + p.off_bar;
     const uint32_t bar_empty = bar_full + 8 * S;
-    const uint32_t bar_tfull = bar_empty + 8 * S;
-    const uint32_t bar_tempty = bar_tfull + 8;
-    const uint32_t bar_drain = bar_tempty + 8;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_bar + 8 * (2 * S + 3));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (2 * S + 3) + 4);
+    const uint32_t bar_tfull = bar_empty + 8 * S;   // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;     // [2]
+    const uint32_t bar_drain = bar_tempty + 16;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_bar + 8 * (2 * S + 5));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (2 * S + 5) + 4);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);    // leader's arrive.expect_tx for both CTAs' bytes
             mbar_init(bar_empty + 8 * s, 1);   // leader's MMA commit, multicast to both CTAs
         }
-        mbar_init(bar_tfull, 1);               // leader's commit after a tile, multicast
-        mbar_init(bar_tempty, 2 * EPI_WARPS);  // epilogue warps of both CTAs (leader's copy is used)
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);               // leader's commit after a tile, multicast
+            mbar_init(bar_tempty + 8 * b, 2 * EPI_WARPS);  // epilogue warps of both CTAs (leader's copy is used)
+        }
         mbar_init(bar_drain, 1);               // leader's final commit, multicast
         *abort_flag = 0;
         fence_mbar_init();
@@ -522,10 +553,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             int st = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (long long pass = 0; ok && pass * G < total; ++pass) {
-                const long long i = item_index(pass, G, pair);
-                if (i >= total) continue;
-                const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
+            ItemStream items(p.plan, p.E, p.tiles_n, nt_per_expert, G, pair, total);
+            Item it;
+            while (ok && items.next(it)) {
                 const int m_row = it.tm * PAIR_M + static_cast<int>(rank) * BM;
                 const int n_row1 = it.tn * p.tn + static_cast<int>(rank) * h1;
                 const int n_row2 = it.tn * p.tn + p.n1 + static_cast<int>(rank) * h2;
@@ -584,10 +614,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             uint32_t c = 0;
             bool live = true;
             const bool gate = p.sf_slots < S;
-            for (long long pass = 0; pass * G < total; ++pass) {
-                const long long i = item_index(pass, G, pair);
-                if (i >= total) continue;
-                const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
+            ItemStream items(p.plan, p.E, p.tiles_n, nt_per_expert, G, pair, total);
+            Item it;
+            while (items.next(it)) {
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
                     const uint32_t st = c % S;
                     if (c >= static_cast<uint32_t>(S)) named_bar_sync(BAR_FREE + st, 64);  // MMA warp took the previous fill
@@ -623,89 +652,125 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         const int ncols = p.tn >> 1;
         const int nchunks = (ncols + 31) >> 5;
         const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
-        const bool odd = lane & 1;
-        uint32_t tiles = 0;
-        for (long long pass = 0; pass * G < total; ++pass) {
-            const long long i = item_index(pass, G, pair);
-            if (i >= total) continue;
-            const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
-            const int mrow = it.tm * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;  // this lane's M-side row
-            const int ncol0 = it.tn * p.tn + h * ncols;                                      // first N-side row here
-            // NK: a lane owns output row mrow; KN: a lane owns output column
-            // mrow, and lane pairs share the column pair (k2, k2 + 1)
-            const int k2 = mrow & ~1;
-            const bool row_in = p.kn ? (k2 < p.K) : (mrow < p.N);
-            uint16_t* obase = p.kn ? p.out + static_cast<size_t>(it.g) * p.N * static_cast<size_t>(p.K) + k2
-                                   : p.out + (static_cast<size_t>(it.g) * p.N + mrow) * static_cast<size_t>(p.K) + ncol0;
-            // Narrow one 32-column chunk (columns 32 j .. 32 j + 31 of this warp's
-            // half) to bf16 and store it. NK: 16-byte runs of the lane's row.
-            // KN: neighbouring lanes swap their (n, n+1) pairs so that the even
-            // lane stores (k, k+1) of row n and the odd lane (k, k+1) of row
-            // n+1: 4-byte stores, 64 contiguous bytes per row and instruction.
-            auto store_chunk = [&](int j, const uint32_t (&v)[32]) {
-                if (!p.kn) {
+        // the loop is instantiated per accumulator count (1 or 2), which keeps
+        // the buffer index out of the registers the TMEM loads need
+        auto epilogue_loop = [&](auto nbuf_tag, auto mode_tag) {
+            constexpr uint32_t BUF_SHIFT = decltype(nbuf_tag)::value == 2 ? 1u : 0u;
+            // 0: rows of A on the 256 side, 16-byte stores; 1: the same with
+            // 32-byte stores; 2: rows of B on the 256 side (transposed stores)
+            constexpr int MODE = decltype(mode_tag)::value;
+            uint32_t ntile = 0;  // non-empty tiles drained so far
+            const bool odd = lane & 1;
+            // (no look-ahead here: the item's loads overlap the wait for its
+            // accumulator; 32-bit counters: the item count is below 2^31)
+            const int total32 = static_cast<int>(total);
+            for (int pass = 0; pass * G < total32; ++pass) {
+                const int i = (pass & 1) ? pass * G + (G - 1 - pair) : pass * G + pair;
+                if (i >= total32) continue;
+                const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
+                const int mrow = it.tm * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;  // this lane's M-side row
+                const int ncol0 = it.tn * p.tn + h * ncols;                                      // first N-side row here
+                // NK: a lane owns output row mrow; KN: a lane owns output column
+                // mrow, and lane pairs share the column pair (k2, k2 + 1)
+                const int k2 = mrow & ~1;
+                const bool row_in = MODE == 2 ? (k2 < p.K) : (mrow < p.N);
+                uint16_t* obase = MODE == 2 ? p.out + static_cast<size_t>(it.g) * p.N * static_cast<size_t>(p.K) + k2
+                                       : p.out + (static_cast<size_t>(it.g) * p.N + mrow) * static_cast<size_t>(p.K) + ncol0;
+                // Narrow one 32-column chunk (columns 32 j .. 32 j + 31 of this warp's
+                // half) to bf16 and store it. NK: 16-byte runs of the lane's row.
+                // KN: neighbouring lanes swap their (n, n+1) pairs so that the even
+                // lane stores (k, k+1) of row n and the odd lane (k, k+1) of row
+                // n+1: 4-byte stores, 64 contiguous bytes per row and instruction.
+                auto store_chunk = [&](int j, const uint32_t (&v)[32]) {
+                    if (MODE == 1) {
+                        // one full 32-byte sector per lane and store
 #pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        const int cc = 32 * j + c;
-                        if (row_in && cc < ncols && ncol0 + cc < p.K)
-                            *reinterpret_cast<uint4*>(obase + cc) =
-                                make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
-                                           pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
-                    }
-                } else {
+                        for (int c = 0; c < 32; c += 16) {
+                            const int cc = 32 * j + c;
+                            if (row_in && cc < ncols && ncol0 + cc < p.K)
+                                st_global_v8(obase + cc, pack_bf16x2(v[c + 0], v[c + 1]),
+                                             pack_bf16x2(v[c + 2], v[c + 3]), pack_bf16x2(v[c + 4], v[c + 5]),
+                                             pack_bf16x2(v[c + 6], v[c + 7]), pack_bf16x2(v[c + 8], v[c + 9]),
+                                             pack_bf16x2(v[c + 10], v[c + 11]), pack_bf16x2(v[c + 12], v[c + 13]),
+                                             pack_bf16x2(v[c + 14], v[c + 15]));
+                        }
+                    } else if (MODE == 0) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const int cc = 32 * j + c;
-                        if (cc < ncols) {  // the same for the whole warp
-                            const uint32_t mine = pack_bf16x2(v[c], v[c + 1]);
-                            const uint32_t got = __shfl_xor_sync(0xffffffffu, mine, 1);
-                            // even: (own n, partner n) = row n; odd: (partner n+1, own n+1) = row n+1
-                            const uint32_t w = odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
-                            const int n = ncol0 + cc + (odd ? 1 : 0);
-                            if (row_in && n < p.N) *reinterpret_cast<uint32_t*>(obase + static_cast<size_t>(n) * p.K) = w;
+                        for (int c = 0; c < 32; c += 8) {
+                            const int cc = 32 * j + c;
+                            if (row_in && cc < ncols && ncol0 + cc < p.K)
+                                *reinterpret_cast<uint4*>(obase + cc) =
+                                    make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
+                                               pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const int cc = 32 * j + c;
+                            if (cc < ncols) {  // the same for the whole warp
+                                const uint32_t mine = pack_bf16x2(v[c], v[c + 1]);
+                                const uint32_t got = __shfl_xor_sync(0xffffffffu, mine, 1);
+                                // even: (own n, partner n) = row n; odd: (partner n+1, own n+1) = row n+1
+                                const uint32_t w = odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
+                                const int n = ncol0 + cc + (odd ? 1 : 0);
+                                if (row_in && n < p.N) *reinterpret_cast<uint32_t*>(obase + static_cast<size_t>(n) * p.K) = w;
+                            }
                         }
                     }
-                }
-            };
-            if (it.nsteps == 0) {
-                // expert without tokens: an exact +0.0 tile, no accumulator involved
-                uint32_t z[32];
+                };
+                if (it.nsteps == 0) {
+                    // expert without tokens: an exact +0.0 tile, no accumulator involved
+                    uint32_t z[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) z[c] = 0u;
-                for (int j = 0; j < nchunks; ++j) store_chunk(j, z);
-                continue;
-            }
-            // one lane waits, the warp follows its verdict (the TMEM loads below
-            // are warp-collective, so the lanes must not split on a timeout)
-            bool ready = true;
-            if (lane == 0) ready = wait_phase(bar_tfull, tiles & 1, abort_flag, p.wait_ns);
-            if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
-            tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * ncols);
-            auto release = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    // this CTA's accumulator half may be overwritten
-                    if (leader) mbar_arrive(bar_tempty);
-                    else mbar_arrive_cluster(tempty_leader);
+                    for (int c = 0; c < 32; ++c) z[c] = 0u;
+                    for (int j = 0; j < nchunks; ++j) store_chunk(j, z);
+                    continue;
                 }
-            };
+                // one lane waits, the warp follows its verdict (the TMEM loads below
+                // are warp-collective, so the lanes must not split on a timeout)
+                bool ready = true;
+                const uint32_t buf = ntile & BUF_SHIFT, acc_phase = (ntile >> BUF_SHIFT) & 1u;
+                if (lane == 0) ready = wait_phase(bar_tfull + 8 * buf, acc_phase, abort_flag, p.wait_ns);
+                if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * static_cast<uint32_t>(p.tn) + static_cast<uint32_t>(h * ncols);
+                auto release = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // this CTA's half of the accumulator may be overwritten
+                        if (leader) mbar_arrive(bar_tempty + 8 * buf);
+                        else mbar_arrive_cluster(tempty_leader + 8 * buf);
+                    }
+                };
 #pragma unroll 1
-            for (int j0 = 0; j0 < nchunks; j0 += 4) {
-                uint32_t v[4][32];
+                for (int j0 = 0; j0 < nchunks; j0 += 4) {
+                    uint32_t v[4][32];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (j0 + j < nchunks) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
-                tmem_wait_ld();
+                    for (int j = 0; j < 4; ++j)
+                        if (j0 + j < nchunks) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-                if (j0 + 4 >= nchunks) release();
+                    for (int j = 0; j < 4; ++j) reg_fence(v[j]);
+                    if (j0 + 4 >= nchunks) release();
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (j0 + j < nchunks) store_chunk(j0 + j, v[j]);
+                    for (int j = 0; j < 4; ++j)
+                        if (j0 + j < nchunks) store_chunk(j0 + j, v[j]);
+                }
+                ++ntile;
             }
-            ++tiles;
+        };
+        using I1 = std::integral_constant<int, 1>;
+        using I2 = std::integral_constant<int, 2>;
+        using I0 = std::integral_constant<int, 0>;
+        switch ((p.acc_bufs == 2 ? 3 : 0) + (p.kn ? 2 : (p.wide_stores ? 1 : 0))) {
+            case 0: epilogue_loop(I1{}, I0{}); break;
+            case 1: epilogue_loop(I1{}, I1{}); break;
+            case 2: epilogue_loop(I1{}, I2{}); break;
+            case 3: epilogue_loop(I2{}, I0{}); break;
+            case 4: epilogue_loop(I2{}, I1{}); break;
+            default: epilogue_loop(I2{}, I2{}); break;
         }
     }
 
@@ -724,29 +789,36 @@ namespace {
 // Shared-memory and TMEM geometry of the main kernel for an N-side tile of
 // tn rows; false if it does not fit.
 struct Geometry {
-    int stages, sf_slots;
+    int stages, sf_slots, acc_bufs;
+    uint32_t sf_col0;
     uint32_t off_b, off_sfa, off_sfb, off_bar, b_stage, smem_bytes;
 };
 
+// TMEM: one or two accumulators of tn columns, then the scale-factor slots.
+// Two accumulators when they fit beside one slot per stage (tn <= 224 with
+// 6-7 stages), else one with as many slots as fit (at least 2).
 bool geometry(int tn, Geometry* g) {
     const int nblk = (tn + 127) / 128;
     const uint32_t b_stage = static_cast<uint32_t>(tn / 2) * BK;  // multiple of 1024 (tn % 16 == 0)
     const uint32_t per_stage = A_STAGE + b_stage + SF_ATOM + nblk * SF_ATOM + 16;  // + two mbarriers
-    const uint32_t fixed = 1024 + 3 * 8 + 16;  // alignment slack, tile barriers, abort flag / TMEM slot
+    const uint32_t fixed = 1024 + 5 * 8 + 16;  // alignment slack, tile barriers, abort flag / TMEM slot
     int stages = static_cast<int>((MAIN_SMEM_MAX - fixed) / per_stage);
     if (stages > MAX_STAGES) stages = MAX_STAGES;
     const int sf_cols = 4 + 4 * nblk;
-    int slots = (static_cast<int>(TMEM_COLS) - tn) / sf_cols;
+    int bufs = (2 * tn + stages * sf_cols <= static_cast<int>(TMEM_COLS)) ? 2 : 1;
+    int slots = (static_cast<int>(TMEM_COLS) - bufs * tn) / sf_cols;
     if (slots > stages) slots = stages;
     if (stages < 3 || slots < 2) return false;
     g->stages = stages;
     g->sf_slots = slots;
+    g->acc_bufs = bufs;
+    g->sf_col0 = static_cast<uint32_t>(bufs * tn);
     g->b_stage = b_stage;
     g->off_b = static_cast<uint32_t>(stages) * A_STAGE;
     g->off_sfa = g->off_b + stages * b_stage;
     g->off_sfb = g->off_sfa + stages * SF_ATOM;
     g->off_bar = g->off_sfb + stages * nblk * SF_ATOM;
-    g->smem_bytes = g->off_bar + 8 * (2 * stages + 3) + 16 + 1024;
+    g->smem_bytes = g->off_bar + 8 * (2 * stages + 5) + 16 + 1024;
     return g->smem_bytes <= static_cast<uint32_t>(MAIN_SMEM_MAX);
 }
 
@@ -780,12 +852,17 @@ TileConfig make_config(int kn, int tn, int rows_m, int rows_n) {
 }
 
 // Best tile of one orientation: the modelled time of all tiles of an expert
-// of `steps` K-steps over every admissible tn; ties keep the larger tn. The
-// measured column costs include the tile hand-overs at 65-130 K-steps per
-// tile; a tile wider than 256 hands over more slowly (its epilogue stores
-// half of its columns before loading the rest), worth about three more
-// K-steps. The 256 side on B measured about 5% slower (4-byte pair stores).
-TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, double* cost) {
+// of `steps` K-steps over every admissible tn; ties keep the larger tn. In
+// units of one K-step of one output column at tn = 256, a tile costs
+//   max(steps x tn x column_cost(tn), W x tn) + 205,
+// measured on GB300: the column costs include the tile hand-overs at 65-130
+// K-steps per tile, plus three K-steps when a one-accumulator tile is wider
+// than 256 (its epilogue stores half of its columns before loading the
+// rest); W is the output-write floor of a short tile (its 256 x tn bf16
+// stores: about 6.6 K-steps with 32-byte stores, 13 with 16-byte ones, 17 for
+// the transposed 4-byte stores of the 256 side on B), 205 a fixed per-tile
+// cost. The 256 side on B also measured about 8% slower on long tiles.
+TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, bool wide_ok, double* cost) {
     TileConfig best{};
     double best_cost = -1.0;
     for (int tn = MAX_TN; tn >= 16; tn -= 16) {
@@ -793,9 +870,11 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, d
         Geometry g;
         if (!geometry(tn, &g)) continue;
         const TileConfig tc = make_config(kn, tn, rows_m, rows_n);
-        const double epi = kn ? 1.05 : 1.0;
-        const double c = static_cast<double>(tc.tiles_m) * tc.tiles_n * tn * column_cost(tn) * epi *
-                         (steps + (tn > 256 ? 3.0 : 0.0));
+        const bool wide = !kn && wide_ok && tn % 32 == 0;
+        const double w_floor = kn ? 17.0 : (wide ? 6.6 : 13.0);
+        const double run = (steps + (g.acc_bufs == 1 && tn > 256 ? 3.0 : 0.0)) * tn * column_cost(tn) * (kn ? 1.08 : 1.0);
+        const double per_tile = (run > w_floor * tn ? run : w_floor * tn) + 205.0;
+        const double c = static_cast<double>(tc.tiles_m) * tc.tiles_n * per_tile;
         if (best_cost < 0 || c < best_cost * (1.0 - 1e-9)) {
             best_cost = c;
             best = tc;
@@ -812,8 +891,9 @@ bool choose_tiles(int N, int K, int E, int64_t M, int force, int force_tn, TileC
     if (force_tn && (force_tn < 16 || force_tn > MAX_TN || force_tn % 16)) return false;
     const double steps = (E > 0 && M > 0) ? static_cast<double>(M) / (static_cast<double>(E) * BK) + 1.0 : 32.0;
     double c_nk, c_kn;
-    const TileConfig nk = best_of(0, N, K, steps, force_tn, &c_nk);
-    const TileConfig kn = best_of(1, K, N, steps, force_tn, &c_kn);
+    // 32-byte output stores need 16-column-aligned output rows (K % 16 == 0)
+    const TileConfig nk = best_of(0, N, K, steps, force_tn, K % 16 == 0, &c_nk);
+    const TileConfig kn = best_of(1, K, N, steps, force_tn, K % 16 == 0, &c_kn);
     if (c_nk < 0 || c_kn < 0) return false;
     if (force == 1) *tc = nk;
     else if (force == 2) *tc = kn;
@@ -829,6 +909,8 @@ bool ws_layout(int E, int N, int K, int64_t M, const TileConfig& tc, WsLayout* L
     const int64_t rows_m = static_cast<int64_t>(tc.tiles_m) * ts * 2;
     const int64_t rows_n = static_cast<int64_t>(tc.tiles_n) * ts * tc.nblk_n;
     if (rows_m > (int64_t(1) << 31) - 1 || rows_n > (int64_t(1) << 31) - 1) return false;
+    // work items (expert, tile) are counted in 32-bit integers in the kernel
+    if (static_cast<int64_t>(E) * tc.tiles_m * tc.tiles_n > (int64_t(1) << 31) - 1) return false;
     L->ts_max = static_cast<int>(ts);
     L->tc = tc;
     const size_t plan_bytes = sizeof(int32_t) * (PLAN_HDR + 5 * static_cast<size_t>(E));
@@ -927,6 +1009,9 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     mp.kn = tc.kn;
     mp.stages = geo.stages;
     mp.sf_slots = geo.sf_slots;
+    mp.acc_bufs = geo.acc_bufs;
+    mp.wide_stores = (!tc.kn && tc.tn % 32 == 0 && a.K % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;
+    mp.sf_col0 = geo.sf_col0;
     mp.off_b = geo.off_b;
     mp.off_sfa = geo.off_sfa;
     mp.off_sfb = geo.off_sfb;

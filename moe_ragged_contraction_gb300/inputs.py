@@ -29,6 +29,12 @@ Recipes (numpy ``default_rng(seed)``):
   units; the residual goes to the last ramp entry; a seeded permutation places
   them and leaves one expert empty.
 
+* ``manyE160`` (1005) / ``manyE512`` (1006): many experts with few tokens each,
+  balanced routing in 32-token units ("Group-GEMM in XLA", Part 4: balanced
+  group sizes; expert counts and feature sizes of its micro-benchmark classes
+  with 160 and 512 experts, token counts raised to whole 32-token scale
+  blocks: 64 and 32 tokens per expert).
+
 Operands: dY [M,N] and X [M,K] are drawn directly as their token-contiguous
 transposes A_f32 [N,M] and B_f32 [K,M]; N(0,1) for every workload but
 ``671Bd``, which draws Student-t with 3 degrees of freedom, generated from its
@@ -70,6 +76,11 @@ WORKLOADS = {
                        "671B up/gate: E=32 N=4096 K=7168 M=262144, Zipf routing max/mean~1.7, two empty experts"),
     "671Bd": Workload("671Bd", 32, 7168, 2048, 524288, 1004, "student_t3",
                       "671B down: E=32 N=7168 K=2048 M=524288, ramp routing max/mean~1.5, odd 32-multiples, one empty, Student-t(3) operands"),
+    # many experts, few tokens each (scheduling and output-write stress)
+    "manyE160": Workload("manyE160", 160, 1536, 5120, 10240, 1005, "normal",
+                         "many-expert stress: E=160 N=1536 K=5120 M=10240, balanced routing, 64 tokens per expert"),
+    "manyE512": Workload("manyE512", 512, 512, 2048, 16384, 1006, "normal",
+                         "many-expert stress: E=512 N=512 K=2048 M=16384, balanced routing, 32 tokens per expert"),
 }
 
 
@@ -143,12 +154,18 @@ def _sizes_ramp_odd(w: Workload, rng, n_nonempty=31, ratio=1.5) -> np.ndarray:
     return sizes
 
 
+def _sizes_balanced(w: Workload, rng) -> np.ndarray:
+    return balanced_sizes(w.E, w.M)
+
+
 _RECIPES = {
     "tiny": _sizes_tiny,
     "16B": _sizes_ramp_offset,
     "16Bp": _sizes_ramp_offset,
     "671Bgu": _sizes_zipf,
     "671Bd": _sizes_ramp_odd,
+    "manyE160": _sizes_balanced,
+    "manyE512": _sizes_balanced,
 }
 
 

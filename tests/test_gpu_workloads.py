@@ -24,7 +24,7 @@ def built():
     mx.load()
 
 
-@pytest.mark.parametrize("name", ["tiny", "16B", "16Bp", "671Bgu", "671Bd"])
+@pytest.mark.parametrize("name", ["tiny", "16B", "16Bp", "671Bgu", "671Bd", "manyE160", "manyE512"])
 def test_workload_parity(name):
     w = I.WORKLOADS[name]
     A, sA, B, sB, offs = workload_inputs(name)
