@@ -205,6 +205,14 @@ def cpu_oracle_rate(A, sA, B, sB, offs, w, target_s: float, threads: int, seed: 
     return flop / dt / 1e12, dt, desc
 
 
+def hold_gpu(steps: int) -> None:
+    """Keep the current stream busy for about 0.2 ms per step that follows
+    (a spin kernel), long enough for the host to enqueue them."""
+    import torch
+
+    torch.cuda._sleep(int(4e5 * steps))
+
+
 def bench_gpu(args):
     import torch
 
@@ -263,7 +271,11 @@ def bench_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     # the timed steps run the plain product call (its main kernel is launched
-    # as a programmatic dependent of the prep kernel and overlaps its tail)
+    # as a programmatic dependent of the prep kernel and overlaps its tail).
+    # A device-side sleep first keeps the GPU busy while the host enqueues all
+    # K steps, so each step's events bracket device time only, not the host's
+    # per-call enqueue latency (the end-to-end figure below includes that).
+    hold_gpu(K)
     for i in range(K):
         flush.zero_()
         ev[i][0].record(stream)
@@ -277,6 +289,7 @@ def bench_gpu(args):
     # the main kernel's own duration: the same steps again with events recorded
     # right before and after its launch (which serialises it behind the prep
     # kernel, so this is its full launch-to-end time)
+    hold_gpu(K)
     for i in range(K):
         flush.zero_()
         step(main_pair=evm[i])

@@ -59,19 +59,42 @@ struct PrepSide {
     int blocks;            // 128-row blocks per tile: ceil(tile_rows / 128)
 };
 
-// Every block first rebuilds the per-expert runs from offs (one warp, shuffle
-// scans; 3E + 1 words of shared memory). Block 0 also writes the plan. Then
-// the blocks stride over gather tasks (below), writing the 512-byte
-// scale-factor blocks: block h of tile t of a side holds rows
-// t * tile_rows + 128 h + r (r < 128; zero past the tile or the plane), and
-// row r, 32-token block kb sits at byte (r % 32) * 16 + (r / 32) * 4 + kb.
-// Blocks: the M side's tiles * blocks first, then the N side's.
+// Four scale bytes starting at byte `off` of the plane (which holds `size`
+// bytes): one aligned 32-bit load, or two and a funnel shift when the bytes
+// straddle a word (alignment is taken on the absolute address, so an
+// unaligned plane is fine: rounding down never leaves its allocation); byte
+// loads where a word would run past the end of the plane.
+__device__ __forceinline__ uint32_t load_scale4(const uint8_t* __restrict__ plane, size_t off, size_t size) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(plane) + off;
+    const uintptr_t w = a & ~uintptr_t(3);
+    const uint32_t sh = static_cast<uint32_t>(a & 3) * 8;
+    const uintptr_t end = reinterpret_cast<uintptr_t>(plane) + size;
+    if (w + (sh ? 8 : 4) <= end) {
+        const uint32_t lo = __ldg(reinterpret_cast<const uint32_t*>(w));
+        if (sh == 0) return lo;
+        const uint32_t hi = __ldg(reinterpret_cast<const uint32_t*>(w + 4));
+        return __funnelshift_r(lo, hi, sh);
+    }
+    uint32_t v = 0;
+    for (int kb = 0; kb < 4; ++kb)
+        if (off + kb < size) v |= static_cast<uint32_t>(__ldg(plane + off + kb)) << (8 * kb);
+    return v;
+}
+
+// Every block first rebuilds the per-expert runs from offs (staged in shared
+// memory by all threads, then scanned by one warp with shuffles; 3E + 1
+// words of shared memory). Block 0 also writes the plan. Then the blocks
+// stride over gather tasks (below), writing the 512-byte scale-factor blocks:
+// block h of tile t of a side holds rows t * tile_rows + 128 h + r (r < 128;
+// zero past the tile or the plane), and row r, 32-token block kb sits at byte
+// (r % 32) * 16 + (r / 32) * 4 + kb. Blocks: the M side's tiles * blocks
+// first, then the N side's.
 __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs, const PrepSide sm_side,
                                                            const PrepSide sn_side, int32_t* __restrict__ plan, int E,
                                                            long long M, int ts_max) {
     extern __shared__ int prep_smem[];
     int* s_start = prep_smem;        // [E]
-    int* s_end = s_start + E;        // [E]
+    int* s_end = s_start + E;        // [E]: raw offs first, then the clamped ends
     int* s_sb = s_end + E;           // [E + 1]: first global K-step of each expert, then the total
     __shared__ int s_flags;
 
@@ -79,13 +102,15 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     const unsigned full = 0xffffffffu;
     const int Mi = static_cast<int>(M);
 
+    for (int g = threadIdx.x; g < E; g += PREP_THREADS) s_end[g] = offs[g];
+    __syncthreads();
     if (warp == 0) {
         int carry_end = 0, carry_steps = 0, flags = 0;
         for (int base = 0; base < E; base += 32) {
             const int g = base + lane;
             int o = 0;
             if (g < E) {
-                o = offs[g];
+                o = s_end[g];
                 if (o < 0) { o = 0; flags |= MXFP8_DEV_OFFS_RANGE; }
                 if (o > Mi) { o = Mi; flags |= MXFP8_DEV_OFFS_RANGE; }
                 if (o & 31) { o &= ~31; flags |= MXFP8_DEV_OFFS_ALIGN; }
@@ -107,6 +132,7 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
                 int t = __shfl_up_sync(full, incl, d);
                 if (lane >= d) incl += t;
             }
+            __syncwarp();
             if (g < E) {
                 s_start[g] = start;
                 s_end[g] = end;
@@ -148,12 +174,13 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         }
     }
 
-    // Scale-factor gather as a tile transpose: a task is (128-row block, 32
-    // consecutive global K-steps). Lane l of a warp owns K-step gs0 + l and
-    // loads that step's 4 scale bytes of one row, so consecutive lanes read
-    // consecutive 4-byte groups of the row (coalesced within an expert); the
-    // words are staged in a padded [128][33] shared tile, then each 512-byte
-    // block is written by one warp with 16-byte stores.
+    // Scale-factor gather as a tile transpose. A task is (128-row block, 32
+    // consecutive global K-steps): lane l owns K-step gs0 + l, finds its
+    // expert, and reads that step's (up to) 4 scale bytes of each row with one
+    // or two aligned 32-bit loads, so a warp reads a contiguous run of each
+    // row within an expert. The words are staged in a padded [128][33] shared
+    // tile, then each 512-byte block is written by one warp with 16-byte
+    // stores.
     uint32_t* tile = reinterpret_cast<uint32_t*>(s_sb + E + 1);  // [PREP_ROWS][PREP_TILE_STEPS + 1]
     const int nchunks = (TS + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS;
     const int mblocks = sm_side.tiles * sm_side.blocks;
@@ -164,11 +191,15 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         const int hb = static_cast<int>(task / nchunks);
         const int gs0 = static_cast<int>(task - static_cast<long long>(hb) * nchunks) * PREP_TILE_STEPS;
         const bool mside = hb < mblocks;
-        const PrepSide& sd = mside ? sm_side : sn_side;
+        const uint8_t* plane = mside ? sm_side.plane : sn_side.plane;
+        uint8_t* sf = mside ? sm_side.sf : sn_side.sf;
+        const int rows = mside ? sm_side.rows : sn_side.rows;
+        const int tile_rows = mside ? sm_side.tile_rows : sn_side.tile_rows;
+        const int blocks = mside ? sm_side.blocks : sn_side.blocks;
         const int local = mside ? hb : hb - mblocks;
-        const int t = local / sd.blocks, h = local - t * sd.blocks;
+        const int t = local / blocks, h = local - t * blocks;
         const int in_tile0 = PREP_ROWS * h;  // first row of this block inside its tile
-        const int row0 = t * sd.tile_rows + in_tile0;
+        const int row0 = t * tile_rows + in_tile0;
         // this lane's K-step: its expert, first scale column and valid 32-token blocks
         const int gs = gs0 + lane;
         long long col = 0;
@@ -184,27 +215,20 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
             const long long left = (static_cast<long long>(s_end[lo]) - t0 + 31) >> 5;
             nvalid = static_cast<int>(left < 4 ? left : 4);
         }
-        // all of this warp's rows are loaded before any is stored, so the
-        // loads of a task are in flight together (one memory latency, not 16)
+        const uint32_t keep = nvalid >= 4 ? 0xffffffffu : ((1u << (8 * nvalid)) - 1u);
+        const size_t plane_bytes = static_cast<size_t>(rows) * static_cast<size_t>(sM);
         constexpr int ROWS_PER_WARP = PREP_ROWS / (PREP_THREADS / 32);
-        uint8_t bv[ROWS_PER_WARP][4];
+        uint32_t wv[ROWS_PER_WARP];
 #pragma unroll
         for (int i = 0; i < ROWS_PER_WARP; ++i) {
             const int r = warp + i * (PREP_THREADS / 32);
             const int row = row0 + r;
-            const bool ok = in_tile0 + r < sd.tile_rows && row < sd.rows;
-            const uint8_t* src = sd.plane + static_cast<size_t>(ok ? row : 0) * sM + col;
-#pragma unroll
-            for (int kb = 0; kb < 4; ++kb) bv[i][kb] = (ok && kb < nvalid) ? __ldg(src + kb) : uint8_t(0);
+            const bool ok = nvalid > 0 && in_tile0 + r < tile_rows && row < rows;
+            wv[i] = ok ? (load_scale4(plane, static_cast<size_t>(row) * sM + col, plane_bytes) & keep) : 0u;
         }
 #pragma unroll
-        for (int i = 0; i < ROWS_PER_WARP; ++i) {
-            const int r = warp + i * (PREP_THREADS / 32);
-            tile[r * (PREP_TILE_STEPS + 1) + lane] = static_cast<uint32_t>(bv[i][0]) |
-                                                     (static_cast<uint32_t>(bv[i][1]) << 8) |
-                                                     (static_cast<uint32_t>(bv[i][2]) << 16) |
-                                                     (static_cast<uint32_t>(bv[i][3]) << 24);
-        }
+        for (int i = 0; i < ROWS_PER_WARP; ++i)
+            tile[(warp + i * (PREP_THREADS / 32)) * (PREP_TILE_STEPS + 1) + lane] = wv[i];
         __syncthreads();
         // block j of this task: lane r0 writes rows r0, r0+32, r0+64, r0+96 (16 bytes)
         for (int j = warp; j < PREP_TILE_STEPS; j += PREP_THREADS / 32) {
@@ -214,7 +238,7 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
             o.y = tile[(lane + 32) * (PREP_TILE_STEPS + 1) + j];
             o.z = tile[(lane + 64) * (PREP_TILE_STEPS + 1) + j];
             o.w = tile[(lane + 96) * (PREP_TILE_STEPS + 1) + j];
-            uint8_t* dst = sd.sf + ((static_cast<size_t>(t) * ts_max + gs0 + j) * sd.blocks + h) * SF_ATOM;
+            uint8_t* dst = sf + ((static_cast<size_t>(t) * ts_max + gs0 + j) * blocks + h) * SF_ATOM;
             reinterpret_cast<uint4*>(dst)[lane] = o;
         }
         __syncthreads();
@@ -961,6 +985,14 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
                                 ((L.ts_max + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS);
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
                           sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
+        // (large E can need more than the 48 KB default of shared memory)
+        static bool prep_attr[64] = {};
+        if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
+        if (!prep_attr[a.dev]) {
+            cudaError_t e0 = cudaFuncSetAttribute(wgrad_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+            if (e0 != cudaSuccess) return e0;
+            prep_attr[a.dev] = true;
+        }
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wgrad_prep, PREP_THREADS, sm);
         if (e != cudaSuccess) return e;

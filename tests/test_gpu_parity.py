@@ -306,3 +306,42 @@ def test_tilings_exact_integers(tiling_reset):
         mx.set_tile_rows(tn)
         got = run_gpu(A, sA, B, sB, offs, E, N, K)
         assert same_bits_signless_zero(got, ref), f"tiling mode={mode} tn={tn}"
+
+
+# ------------------------------------------------------------------ extremes of the plan
+
+def test_max_expert_count():
+    """E = 2048 (the largest supported): the plan, the scale gather and the
+    schedule at their largest expert count, with empty and 32-token experts."""
+    E, N, K = 2048, 64, 128
+    rng = np.random.default_rng(91)
+    sizes = 32 * rng.integers(0, 3, E)
+    M = int(sizes.sum()) + 64  # 64 tokens of padding past the last group
+    A, sA = quantised_operand(N, M, seed=91, stream=0)
+    B, sB = quantised_operand(K, M, seed=91, stream=1)
+    offs = np.cumsum(sizes).astype(np.int32)
+    got = run_gpu(A, sA, B, sB, offs, E, N, K)
+    check_tol(got, A, sA, B, sB, offs, E, N, K, M)
+
+
+def test_unaligned_scale_planes():
+    """Scale planes that start at odd byte addresses (views into larger
+    buffers) give the same bits as aligned ones."""
+    E, N, K, M = 3, 256, 384, 1536
+    A, sA = quantised_operand(N, M, seed=93, stream=0)
+    B, sB = quantised_operand(K, M, seed=93, stream=1)
+    offs = np.array([416, 416, 1504], np.int32)
+    ref = run_gpu(A, sA, B, sB, offs, E, N, K)
+
+    def odd_view(a, shift):
+        buf = torch.empty(a.size + 64, dtype=torch.uint8, device="cuda")
+        v = buf[shift:shift + a.size].view(a.shape)
+        v.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+        return v
+
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    out.view(torch.int16).fill_(-1)
+    mx.wgrad_grouped(dev(A), odd_view(sA, 1), dev(B), odd_view(sB, 3), dev(offs), out=out)
+    torch.cuda.synchronize()
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
