@@ -425,8 +425,8 @@ def bench_comparators(args):
     ms = timed(lambda: mx.wgrad_grouped(A, sA, B, sB, offs, out=out), args.steps)
     res["mxfp8_wgrad_this_library"] = w.flop / (ms * 1e-3) / 1e12
     # BF16 vendor baseline: one cuBLAS bf16 GEMM per expert on the token slice
-    # (torch._grouped_mm is not used: in PyTorch 2.9.1 for aarch64 its
-    # Blackwell kernel is built without TMEM support and fails at launch)
+    # (torch._grouped_mm is not used: it raised a GPU fault in one run on
+    # this hardware)
     a16 = torch.randn(w.N, w.M, device=device, dtype=torch.bfloat16)
     b16 = torch.randn(w.K, w.M, device=device, dtype=torch.bfloat16)
     ends = I.offsets(I.group_sizes(args.config)).tolist()
@@ -462,6 +462,63 @@ def bench_comparators(args):
         res["dense8192_mxfp8_vendor"] = None
         res["dense8192_vendor_error"] = str(e).splitlines()[0][:200]
     return res
+
+
+# ------------------------------------------------------------------ fused quantiser
+
+def bench_quantizer(args):
+    """Opt-in line: the fused bf16 quantise-and-transpose that builds this
+    workload's operands (dY [M, N] and X [M, K], token-major bf16, to
+    A [N, M] and B [K, M] E4M3 plus scales), HBM-bound: GB/s over the
+    algorithmic bytes (2 read + 1 + 1/32 written per element)."""
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    device = torch.device("cuda")
+    mx.build()
+    mx.load()
+    w = I.WORKLOADS[args.config]
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    dy = torch.randn(w.M, w.N, device=device, generator=g).to(torch.bfloat16)
+    x = torch.randn(w.M, w.K, device=device, generator=g).to(torch.bfloat16)
+    qa = torch.empty((w.N, w.M), dtype=torch.uint8, device=device)
+    sa = torch.empty((w.N, w.M // 32), dtype=torch.uint8, device=device)
+    qb = torch.empty((w.K, w.M), dtype=torch.uint8, device=device)
+    sb = torch.empty((w.K, w.M // 32), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step():
+        mx.quantize_transpose_bf16(dy, qa, sa)
+        mx.quantize_transpose_bf16(x, qb, sb)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    hold_gpu(K)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    elems = float(w.M) * (w.N + w.K)
+    alg = elems * (2 + 1 + 1 / 32)
+    _, _, peaks = mxfp8_peak()
+    hbm = float(peaks["hbm_gbs"]) if peaks else HBM_FALLBACK_GBS
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"metric": "GB/s fused bf16 quantise-and-transpose (operands of the wgrad)", "value": gbs,
+            "unit": "GB/s", "ms_per_step": ms, "steps": K, "warmup": args.warmup,
+            "config": {"workload": args.config, "M": w.M, "N": w.N, "K": w.K,
+                       "l2": "flushed (256 MiB write) before every timed step"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "algorithmic_bytes_per_step": alg, "kernel": "quantize_transpose_bf16_kernel"},
+            "gpu_launches": 2 * K}
 
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
@@ -533,11 +590,15 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--comparators", action="store_true",
                     help="print a context line with vendor BF16 grouped / dense MXFP8 GEMM timings instead")
+    ap.add_argument("--quantizer", action="store_true",
+                    help="print a line for the fused bf16 quantise-and-transpose of the workload's operands instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.comparators:
         res = bench_comparators(args)
+    elif args.quantizer:
+        res = bench_quantizer(args)
     else:
         res = bench_reference_arm(args) if args.impl == "reference" else bench_gpu(args)
     if res is not None:

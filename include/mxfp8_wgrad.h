@@ -126,6 +126,18 @@ int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B
  */
 int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, void* stream);
 
+/*
+ * Fused quantise-and-transpose from token-major bf16 (the layout in which the
+ * forward and backward passes produce dY and X): x [M][R] bf16 (bit patterns,
+ * 2-byte aligned) becomes q [R][M] E4M3 with the token axis contiguous
+ * (16-byte aligned) and s [R][M/32] E8M0, by the rule of
+ * mxfp8_quantize_tokenwise applied to the transpose: the operand layout of
+ * mxfp8_wgrad_grouped in one pass ("Ragged MXFP8 Weight Gradients", section 1:
+ * operands quantised along the token axis; quantisation itself is outside the
+ * timed operation there). R >= 1, M >= 32, M % 32 == 0.
+ */
+int mxfp8_quantize_transpose_bf16(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s, void* stream);
+
 /* Message for the last non-zero status returned on the calling thread
  * (thread-local; never NULL). */
 const char* mxfp8_last_error(void);

@@ -13,6 +13,7 @@ from ._lib import (  # noqa: F401
     lib_path,
     load,
     quantize_tokenwise,
+    quantize_transpose_bf16,
     set_tile_orientation,
     set_tile_rows,
     set_timing_events,

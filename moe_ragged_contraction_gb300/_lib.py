@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
         lib.mxfp8_wgrad_grouped_ws.restype = I
         lib.mxfp8_quantize_tokenwise.argtypes = [P, I, L, P, P, P]
         lib.mxfp8_quantize_tokenwise.restype = I
+        lib.mxfp8_quantize_transpose_bf16.argtypes = [P, L, I, P, P, P]
+        lib.mxfp8_quantize_transpose_bf16.restype = I
         lib.mxfp8_last_error.argtypes = []
         lib.mxfp8_last_error.restype = ctypes.c_char_p
         lib.mxfp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), I]
@@ -180,6 +182,25 @@ def quantize_tokenwise(x, q=None, s=None, stream=None):
     _expect(q, torch.uint8, "q")
     _expect(s, torch.uint8, "s")
     check(load().mxfp8_quantize_tokenwise(_ptr(x), R, M, _ptr(q), _ptr(s), _stream(stream)))
+    return q, s
+
+
+def quantize_transpose_bf16(x, q=None, s=None, stream=None):
+    """Fused quantise-and-transpose: x bf16 [M, R] (token-major) ->
+    (q uint8 [R, M] E4M3, token axis contiguous; s uint8 [R, M/32] E8M0)."""
+    import torch
+
+    _expect(x, torch.bfloat16, "x")
+    M, R = x.shape
+    if q is None:
+        q = torch.empty((R, M), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((R, M // 32), dtype=torch.uint8, device=x.device)
+    _expect(q, torch.uint8, "q")
+    _expect(s, torch.uint8, "s")
+    if tuple(q.shape) != (R, M) or tuple(s.shape) != (R, M // 32):
+        raise ValueError(f"q must be [{R}, {M}] and s [{R}, {M // 32}]")
+    check(load().mxfp8_quantize_transpose_bf16(_ptr(x), M, R, _ptr(q), _ptr(s), _stream(stream)))
     return q, s
 
 

@@ -353,6 +353,23 @@ int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8
     return MXFP8_OK;
 }
 
+int mxfp8_quantize_transpose_bf16(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s, void* stream) {
+    if (R < 1) return fail(MXFP8_EINVAL, "R=%d must be >= 1", R);
+    if (M < 32 || (M % 32) != 0) return fail(MXFP8_EINVAL, "M=%lld must be a positive multiple of 32", (long long)M);
+    if (!x || !q || !s) return fail(MXFP8_EINVAL, "null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(x) & 1u) != 0) return fail(MXFP8_EALIGN, "x must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return fail(MXFP8_EALIGN, "q must be 16-byte aligned");
+    if (M / 64 + 1 > 0x7fffffffLL || (R + 127) / 128 > 65535)
+        return fail(MXFP8_EINVAL, "M=%lld, R=%d: too large", (long long)M, R);
+    int dev;
+    DeviceInfo info;
+    int rc = current_device(&dev, &info);
+    if (rc) return rc;
+    cudaError_t e = mxw::launch_quantize_transpose(x, M, R, q, s, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "quantize-transpose kernel");
+    return MXFP8_OK;
+}
+
 const char* mxfp8_last_error(void) { return g_err; }
 
 int mxfp8_device_status(int32_t* status, int clear) {

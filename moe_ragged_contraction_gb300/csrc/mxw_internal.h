@@ -79,6 +79,8 @@ struct WgradArgs {
 cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what);
 
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream);
+cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s,
+                                      cudaStream_t stream);
 
 // Sets the calling thread's mxfp8_last_error() message; returns `code`.
 int set_last_error(int code, const char* msg);

@@ -15,6 +15,17 @@ constexpr int QT_THREADS = 256;
 constexpr int QT_TOKENS_PER_THREAD = 8;
 constexpr int QT_TOKENS_PER_BLOCK = QT_THREADS * QT_TOKENS_PER_THREAD;
 
+// Scale exponent of a 32-element block from the bit pattern of its amax
+// (finite): the smallest e with amax <= 448 * 2^e, clamped to [-127, 127].
+__device__ __forceinline__ int block_exponent(uint32_t amax_bits) {
+    const int eb = static_cast<int>(amax_bits >> 23);
+    if (eb == 0) return -127;  // zero or subnormal amax: below 448 * 2^-127
+    // amax = 1.m * 2^(eb-127) = f * 2^(eb-126) with f = 1.m / 2 in [0.5, 1);
+    // 448 = 0.875 * 2^9, so e = (eb - 126) - 9, plus one when f > 0.875 (1.m > 1.75)
+    const int e = eb - 135 + ((amax_bits & 0x7fffffu) > 0x600000u ? 1 : 0);
+    return max(-127, min(127, e));
+}
+
 // Four consecutive threads cover one 32-token block: each loads 8 floats,
 // the group shares amax through two shuffles, each writes its 8 E4M3 bytes,
 // and the first of the four writes the scale byte.
@@ -45,16 +56,7 @@ __device__ __forceinline__ void quantize_group(const float* __restrict__ x, long
         if (leader) s[row * (M / 32) + (t0 >> 5)] = 0xFF;
         return;
     }
-    int e;
-    const int eb = static_cast<int>(amax_bits >> 23);
-    if (eb == 0) {
-        e = -127;  // zero or subnormal amax: below 448 * 2^-127
-    } else {
-        // amax = 1.m * 2^(eb-127) = f * 2^(eb-126) with f = 1.m / 2 in [0.5, 1);
-        // 448 = 0.875 * 2^9, so e = (eb - 126) - 9, plus one when f > 0.875 (1.m > 1.75)
-        e = eb - 135 + ((amax_bits & 0x7fffffu) > 0x600000u ? 1 : 0);
-        e = max(-127, min(127, e));
-    }
+    const int e = block_exponent(amax_bits);
     // 2^-e as an fp32 (e in [-127, 120] here, so the exponent field is in range)
     const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
     uint32_t lo = 0, hi = 0;
@@ -76,6 +78,136 @@ __global__ void __launch_bounds__(QT_THREADS) quantize_tokenwise_kernel(const fl
                                                                         long long M, uint8_t* __restrict__ q,
                                                                         uint8_t* __restrict__ s) {
     for (long long row = blockIdx.y; row < R; row += gridDim.y) quantize_group(x, M, q, s, row);
+}
+
+// ------------------------------------------------------------------ fused transpose
+
+// Quantise-and-transpose from token-major bf16: x [M][R] (the layout dY and X
+// have in the forward and backward passes) to q [R][M] E4M3 with the token
+// axis contiguous and s [R][M/32], by the same rule as above (bf16 values are
+// exact in fp32). A block handles 128 tokens x 128 features. Each thread
+// loads an 8-token x 8-feature sub-block (eight 16-byte row pieces),
+// transposes it in registers with byte permutes and writes eight 16-byte
+// feature pieces into shared memory (rows of 136 bf16: 272 bytes, so the
+// 16-byte reads below are free of bank conflicts); then each thread
+// quantises two (feature, 32-token block) pairs, writing each block's 32
+// bytes as one full sector.
+constexpr int QX_TOK = 128;
+constexpr int QX_FEAT = 128;
+constexpr int QX_THREADS = 256;
+constexpr int QX_ROW = 136;  // padded shared row (bf16 elements)
+
+__global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(const uint16_t* __restrict__ x,
+                                                                             long long M, int R, int vec,
+                                                                             uint8_t* __restrict__ q,
+                                                                             uint8_t* __restrict__ s) {
+    extern __shared__ __align__(16) uint16_t sT[];  // [QX_FEAT][QX_ROW]
+    const long long t0 = static_cast<long long>(blockIdx.x) * QX_TOK;
+    const int f0 = blockIdx.y * QX_FEAT;
+    const int tid = threadIdx.x;
+    {
+        // thread -> tokens t0 + 8 tg .. +7, features f0 + 8 fg .. +7
+        const int tg = tid & 15, fg = tid >> 4;
+        const int fb = f0 + 8 * fg;
+        uint32_t r[8][4];  // r[i][w]: features (2w, 2w+1) of token i
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const long long tok = t0 + 8 * tg + i;
+            const uint16_t* src = x + tok * R + fb;
+            if (tok < M && (vec & 1) && fb + 8 <= R) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+                r[i][0] = w.x; r[i][1] = w.y; r[i][2] = w.z; r[i][3] = w.w;
+            } else {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t lo = (tok < M && fb + 2 * w < R) ? __ldg(src + 2 * w) : 0u;
+                    const uint32_t hi = (tok < M && fb + 2 * w + 1 < R) ? __ldg(src + 2 * w + 1) : 0u;
+                    r[i][w] = lo | (hi << 16);
+                }
+            }
+        }
+        // feature j, tokens (2w', 2w'+1): the j%2 halves of r[2w'][j/2] and r[2w'+1][j/2]
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+            uint4 c;
+            c.x = __byte_perm(r[0][j >> 1], r[1][j >> 1], sel);
+            c.y = __byte_perm(r[2][j >> 1], r[3][j >> 1], sel);
+            c.z = __byte_perm(r[4][j >> 1], r[5][j >> 1], sel);
+            c.w = __byte_perm(r[6][j >> 1], r[7][j >> 1], sel);
+            *reinterpret_cast<uint4*>(sT + (8 * fg + j) * QX_ROW + 8 * tg) = c;
+        }
+    }
+    __syncthreads();
+    // thread -> feature f0 + (tid % 128), token blocks 2 (tid / 128) and 2 (tid / 128) + 1
+    const int fl = tid & (QX_FEAT - 1);
+    const int f = f0 + fl;
+    if (f >= R) return;
+#pragma unroll 1
+    for (int bb = 0; bb < 2; ++bb) {
+        const int b = 2 * (tid >> 7) + bb;
+        const long long tb = t0 + 32 * b;  // first token of the block
+        if (tb >= M) return;               // M % 32 == 0: a block is all in or all out
+        float v[32];
+        uint32_t amax_bits = 0;
+        const uint4* row = reinterpret_cast<const uint4*>(sT + fl * QX_ROW + 32 * b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 w = row[i];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[8 * i + 2 * k] = __uint_as_float(ws[k] << 16);
+                v[8 * i + 2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax_bits = max(amax_bits, __float_as_uint(v[i]) & 0x7fffffffu);
+        uint8_t* qdst = q + static_cast<long long>(f) * M + tb;
+        uint8_t* sdst = s + static_cast<long long>(f) * (M / 32) + (tb >> 5);
+        uint32_t w[8];
+        uint8_t sbyte;
+        if (amax_bits >= 0x7f800000u) {  // NaN or Inf in the block
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0x7f7f7f7fu;
+            sbyte = 0xFF;
+        } else {
+            const int e = block_exponent(amax_bits);
+            const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+                w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            sbyte = static_cast<uint8_t>(e + 127);
+        }
+        if (vec & 2) {  // q 32-byte aligned: one full sector per store
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(qdst), "r"(w[0]),
+                         "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                         : "memory");
+        } else {
+            reinterpret_cast<uint4*>(qdst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(qdst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        *sdst = sbyte;
+    }
+}
+
+cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s,
+                                      cudaStream_t stream) {
+    // bit 0: 16-byte loads of x rows; bit 1: 32-byte stores of q (M % 32 == 0 keeps every block aligned)
+    const int vec = (((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (R % 8) == 0) ? 1 : 0) |
+                    ((reinterpret_cast<uintptr_t>(q) & 31u) == 0 ? 2 : 0);
+    const long long gx = (M + QX_TOK - 1) / QX_TOK;
+    const int gy = (R + QX_FEAT - 1) / QX_FEAT;
+    if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
+    constexpr size_t smem = sizeof(uint16_t) * QX_FEAT * QX_ROW;  // 34 KB
+    quantize_transpose_bf16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), QX_THREADS, smem,
+                                     stream>>>(x, M, R, vec, q, s);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream) {

@@ -178,3 +178,13 @@ def test_workspace_covers_both_orientations(lib):
     finally:
         mx.set_tile_orientation(0)
     assert lib.mxfp8_wgrad_workspace_bytes(E, N, K, M) == max(need)
+
+
+def test_quantize_transpose_validation(lib):
+    q = lib.mxfp8_quantize_transpose_bf16
+    q.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert q(P, 1024, 0, P, P, None) == _lib.EINVAL       # R < 1
+    assert q(P, 1000, 64, P, P, None) == _lib.EINVAL      # M % 32 != 0
+    assert q(None, 1024, 64, P, P, None) == _lib.EINVAL   # null x
+    assert q(P + 1, 1024, 64, P, P, None) == _lib.EALIGN  # x not 2-byte aligned
+    assert q(P, 1024, 64, P + 8, P, None) == _lib.EALIGN  # q not 16-byte aligned

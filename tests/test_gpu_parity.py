@@ -345,3 +345,36 @@ def test_unaligned_scale_planes():
     torch.cuda.synchronize()
     got = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ fused quantise + transpose
+
+def _bf16_bits(x32):
+    """fp32 -> bf16 bit patterns (round to nearest even), NaN kept NaN."""
+    b = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    r[np.isnan(x32)] = 0x7FC0
+    return r
+
+
+@pytest.mark.parametrize("M,R", [(1024, 256), (96, 200), (64, 13), (2048, 1408)])
+def test_quantize_transpose_bit_exact(M, R):
+    """bf16 [M, R] token-major -> E4M3 [R, M] + E8M0 [R, M/32]: bit-identical
+    to the oracle's quantiser applied to the transpose (bf16 values are exact
+    in fp32). Covers a partial token tile (M % 64 == 32), partial feature tiles,
+    rows not a multiple of 8 (scalar loads), tiny, zero and non-finite blocks."""
+    rng = np.random.default_rng(M + R)
+    x = (rng.standard_normal((M, R)) * np.exp2(rng.integers(-8, 9, (1, R)))).astype(np.float32)
+    x[:32, 0] = 0.0
+    x[32:64, min(1, R - 1)] *= np.float32(1e-38)
+    if R > 3 and M >= 96:
+        x[64:96, 2] = np.float32(448.0 * 2.0 ** 7)
+        x[40, 3] = np.inf
+    bits = _bf16_bits(x)
+    x_exact = (bits.astype(np.uint32) << 16).view(np.float32)  # the values the bf16 bits hold
+    q_ref, s_ref = oracle.quantize_tokenwise(np.ascontiguousarray(x_exact.T))
+    xt = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q, s = mx.quantize_transpose_bf16(xt)
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
