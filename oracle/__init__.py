@@ -12,7 +12,14 @@ on MI355X", section 1 and section 5.5; "Group-GEMM in XLA", Part 3,
                      e4m3(A[n,t]) 2^(sA[n,t/32]-127) * e4m3(B[k,t]) 2^(sB[k,t/32]-127) )
 
 computed in fp64 by ``oracle.c`` (plain triple loop, token order) and rounded
-to bf16 in one step. ``ragged_dot.py`` holds the generic fp64 ragged-dot forms
+to bf16 in one step. ``grouped_gemm`` is the non-contracting form in MXFP8
+("Group-GEMM in XLA", Part 1, "The Ragged-Dot Operation"; the forward and
+data-gradient products of the same expert layer):
+
+    out[t, n] = bf16_rne( sum over k of e4m3(X[t,k]) 2^(sX[t,k/32]-127) *
+                          e4m3(W[g,n,k]) 2^(sW[g,n,k/32]-127) ),  g = group of row t,
+
+rows past offs[E-1] zero. ``ragged_dot.py`` holds the generic fp64 ragged-dot forms
 (non-contracting and contracting) used to pin the worked example of the XLA
 page.
 
@@ -70,6 +77,8 @@ def _load():
         lib.oracle_wgrad.restype = I
         lib.oracle_wgrad_points.argtypes = [P, P, P, P, P, I, I, I, L, P, P, P, L, P, P, P, I]
         lib.oracle_wgrad_points.restype = I
+        lib.oracle_grouped_gemm.argtypes = [P, P, P, P, P, I, L, I, I, P, P, L, P, P, P, I]
+        lib.oracle_grouped_gemm.restype = I
         lib.oracle_quantize_tokenwise.argtypes = [P, L, L, P, P, I]
         lib.oracle_quantize_tokenwise.restype = I
         _lib = lib
@@ -149,6 +158,39 @@ def wgrad_points(A, sA, B, sB, offs, E, N, K, M, g, n, k, want_acc=False, nthrea
                                  nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle_wgrad_points: invalid arguments, offsets or indices")
+    return (out, acc, aacc) if want_acc else out
+
+
+def grouped_gemm(X, sX, W, sW, offs, E, M, N, K, points=None, want_acc=False, nthreads=None):
+    """Non-contracting ragged dot in MXFP8: out[t, n] for every row t of group
+    g = sum_k x(t, k) w(g, n, k); X [M,K], sX [M,K/32], W [E,N,K], sW
+    [E,N,K/32]; rows past offs[E-1] are zero. Returns bf16 bits [M,N] (or [P]
+    for ``points`` = (t, n) index arrays), with ``want_acc`` also the fp64 sums
+    and the fp64 sums of |x*w|."""
+    lib = _load()
+    X = _c(X, np.uint8); sX = _c(sX, np.uint8)
+    W = _c(W, np.uint8); sW = _c(sW, np.uint8)
+    offs = _c(offs, np.int32)
+    assert X.size == M * K and sX.size == M * (K // 32)
+    assert W.size == E * N * K and sW.size == E * N * (K // 32) and offs.size == E
+    if points is None:
+        shape = (M, N)
+        pt = pn = None
+        P = 0
+    else:
+        pt = _c(points[0], np.int64); pn = _c(points[1], np.int64)
+        assert pt.size == pn.size
+        P = pt.size
+        shape = (P,)
+    out = np.empty(shape, dtype=np.uint16)
+    acc = np.empty(shape, dtype=np.float64) if want_acc else None
+    aacc = np.empty(shape, dtype=np.float64) if want_acc else None
+    rc = lib.oracle_grouped_gemm(_ptr(X), _ptr(sX), _ptr(W), _ptr(sW), _ptr(offs), E, M, N, K,
+                                 _ptr(pt) if pt is not None else None, _ptr(pn) if pn is not None else None, P,
+                                 _ptr(out), _ptr(acc) if want_acc else None, _ptr(aacc) if want_acc else None,
+                                 nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_grouped_gemm: invalid arguments, offsets or points")
     return (out, acc, aacc) if want_acc else out
 
 

@@ -291,6 +291,101 @@ int oracle_wgrad_points(const uint8_t* A, const uint8_t* sA, const uint8_t* B, c
     return 0;
 }
 
+/* ------------------------------------------------------------- grouped GEMM */
+
+/* The non-contracting ragged dot ("Group-GEMM in XLA", Part 1, "The Ragged-Dot
+ * Operation"), in MXFP8: the rows of X are cut into E contiguous groups by
+ * offs (inclusive ends), and every row t of group g multiplies the weights of
+ * expert g:
+ *   out[t][n] = bf16_rne( sum_k x(t,k) w(g,n,k) ),
+ *   x(t,k) = e4m3(X[t][k]) 2^(sX[t][k/32] - 127),  w likewise from W[g][n][k],
+ * both operands quantised along the contracted axis k. Rows at or past
+ * offs[E-1] belong to no group and are zero. offs need not be multiples of
+ * 32 (the scale blocks run along k, not t). */
+static int check_row_offs(const int32_t* offs, int E, int64_t M) {
+    int64_t prev = 0;
+    for (int g = 0; g < E; ++g) {
+        int64_t o = offs[g];
+        if (o < prev || o > M) return -1;
+        prev = o;
+    }
+    return 0;
+}
+
+typedef struct {
+    const uint8_t *X, *sX, *W, *sW;
+    const int32_t* offs;
+    int E, N, K;
+    int64_t M;
+    const double *lutA, *lutS;
+    uint16_t* out;
+    double *acc, *absacc;
+    const int64_t *pt, *pn; /* points (NULL: every element) */
+} gemm_ctx;
+
+static int group_of_row(const int32_t* offs, int E, int64_t t) {
+    for (int g = 0; g < E; ++g)
+        if (t < offs[g]) return g;
+    return -1; /* past the last group */
+}
+
+static void gemm_element(const gemm_ctx* c, int64_t t, int64_t n, int64_t o) {
+    int g = group_of_row(c->offs, c->E, t);
+    double acc = 0.0, aacc = 0.0;
+    if (g >= 0) {
+        int64_t sK = c->K / 32;
+        const uint8_t* x = c->X + t * c->K;
+        const uint8_t* sx = c->sX + t * sK;
+        const uint8_t* w = c->W + ((int64_t)g * c->N + n) * c->K;
+        const uint8_t* sw = c->sW + ((int64_t)g * c->N + n) * sK;
+        for (int64_t k = 0; k < c->K; ++k) {
+            double pr = (c->lutA[x[k]] * c->lutS[sx[k / 32]]) * (c->lutA[w[k]] * c->lutS[sw[k / 32]]);
+            acc += pr;
+            aacc += fabs(pr);
+        }
+    }
+    c->out[o] = oracle_bf16_rne(acc);
+    if (c->acc) c->acc[o] = acc;
+    if (c->absacc) c->absacc[o] = aacc;
+}
+
+static void gemm_rows(void* p, int64_t t0, int64_t t1) {
+    gemm_ctx* c = (gemm_ctx*)p;
+    for (int64_t t = t0; t < t1; ++t)
+        for (int64_t n = 0; n < c->N; ++n) gemm_element(c, t, n, t * c->N + n);
+}
+
+static void gemm_points(void* p, int64_t i0, int64_t i1) {
+    gemm_ctx* c = (gemm_ctx*)p;
+    for (int64_t i = i0; i < i1; ++i) gemm_element(c, c->pt[i], c->pn[i], i);
+}
+
+/* Full output out [M][N] bf16 bits (acc/absacc optional fp64 [M][N]); with
+ * pt/pn (P points) only those elements, out[i] for (pt[i], pn[i]). Returns 0,
+ * or -1 on invalid arguments (nothing written). */
+int oracle_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, const uint8_t* sW,
+                        const int32_t* offs, int E, int64_t M, int N, int K,
+                        const int64_t* pt, const int64_t* pn, int64_t P,
+                        uint16_t* out, double* acc, double* absacc, int nthreads) {
+    if (E < 1 || M < 0 || N < 0 || K < 32 || (K % 32) != 0 || !offs) return -1;
+    if (check_row_offs(offs, E, M) != 0) return -1;
+    if (pt) {
+        for (int64_t i = 0; i < P; ++i)
+            if (pt[i] < 0 || pt[i] >= M || pn[i] < 0 || pn[i] >= N) return -1;
+    }
+    double lutA[256], lutS[256];
+    fill_luts(lutA, lutS);
+    gemm_ctx c;
+    c.X = X; c.sX = sX; c.W = W; c.sW = sW; c.offs = offs;
+    c.E = E; c.N = N; c.K = K; c.M = M;
+    c.lutA = lutA; c.lutS = lutS;
+    c.out = out; c.acc = acc; c.absacc = absacc;
+    c.pt = pt; c.pn = pn;
+    if (pt) parallel_for(P, nthreads, gemm_points, &c);
+    else parallel_for(M, nthreads, gemm_rows, &c);
+    return 0;
+}
+
 /* ------------------------------------------------------------- quantiser */
 
 typedef struct {

@@ -421,3 +421,102 @@ def test_quantiser_nonfinite_block(oracle_mod):
     q, s = oracle_mod.quantize_tokenwise(x)
     assert s[0, 0] == 0xFF and s[0, 1] == 0xFF
     assert np.all(q == 0x7F)
+
+
+# --------------------------------------------------------------- non-contracting grouped GEMM
+
+def q_weights(rng, E, N, K):
+    W = np.empty((E, N, K), np.uint8)
+    sW = np.empty((E, N, K // 32), np.uint8)
+    for g in range(E):
+        W[g], sW[g] = q_operand(rng, N, K)
+    return W, sW
+
+
+def exact_grouped_gemm(X, sX, W, sW, offs, E, M, N, K):
+    fa = {c: Fraction(float(torch_e4m3([c])[0])) for c in range(256) if (c & 0x7F) != 0x7F}
+    out = np.zeros((M, N), dtype=np.uint16)
+    lo = 0
+    for g in range(E):
+        hi = int(offs[g])
+        for t in range(lo, hi):
+            for n in range(N):
+                acc = Fraction(0)
+                for k in range(K):
+                    x = fa[int(X[t, k])] * Fraction(2) ** (int(sX[t, k // 32]) - 127)
+                    w = fa[int(W[g, n, k])] * Fraction(2) ** (int(sW[g, n, k // 32]) - 127)
+                    acc += x * w
+                out[t, n] = bf16_nearest_exact(acc)
+        lo = hi
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_grouped_gemm_exact_bruteforce(oracle_mod, seed):
+    """Exact rational sums rounded to bf16, on tiny ragged inputs whose group
+    boundaries are arbitrary rows (not multiples of 32), with an empty group
+    and padding rows past the last group."""
+    rng = np.random.default_rng(300 + seed)
+    E = int(rng.integers(2, 4))
+    M = int(rng.integers(3, 9))
+    N = int(rng.integers(1, 4))
+    K = 32 * int(rng.integers(1, 3))
+    X, sX = q_operand(rng, M, K)
+    W, sW = q_weights(rng, E, N, K)
+    cuts = np.sort(rng.integers(0, M + 1, size=E))
+    cuts[0] = min(cuts[0], cuts[1])  # keep non-decreasing
+    offs = cuts.astype(np.int32)
+    got = oracle_mod.grouped_gemm(X, sX, W, sW, offs, E, M, N, K)
+    ref = exact_grouped_gemm(X, sX, W, sW, offs, E, M, N, K)
+    zero = lambda a: np.where((a & 0x7FFF) == 0, 0, a)  # noqa: E731
+    assert np.array_equal(zero(got), zero(ref))
+    assert np.all(got[int(offs[-1]):] == 0)
+
+
+def test_grouped_gemm_is_ragged_dot_of_dequantised(oracle_mod):
+    """The grouped GEMM is the generic non-contracting ragged dot (per-group
+    numpy matmul) on operands dequantised through the library decode tables:
+    lhs = X [M, K], rhs[g] = W[g]^T [K, N]."""
+    rng = np.random.default_rng(31)
+    E, M, N, K = 3, 50, 7, 96
+    X, sX = q_operand(rng, M, K)
+    W, sW = q_weights(rng, E, N, K)
+    sizes = [17, 0, 29]  # 4 padding rows at the end
+    offs = np.cumsum(sizes).astype(np.int32)
+    _, acc, aacc = oracle_mod.grouped_gemm(X, sX, W, sW, offs, E, M, N, K, want_acc=True)
+
+    def deq(q, s):
+        return torch_e4m3(q.reshape(-1)).reshape(q.shape) * np.repeat(torch_e8m0(s.reshape(-1)).reshape(s.shape), 32, axis=-1)
+
+    Xd = deq(X, sX)
+    Wd = np.stack([deq(W[g], sW[g]) for g in range(E)])
+    ref = rd.ragged_dot(Xd, np.transpose(Wd, (0, 2, 1)), sizes)
+    assert np.allclose(acc, ref, rtol=1e-12, atol=0)
+    ref_abs = rd.ragged_dot(np.abs(Xd), np.abs(np.transpose(Wd, (0, 2, 1))), sizes)
+    assert np.allclose(aacc, ref_abs, rtol=1e-12, atol=0)
+
+
+def test_grouped_gemm_single_group_is_dense(oracle_mod):
+    rng = np.random.default_rng(32)
+    M, N, K = 40, 9, 64
+    X, sX = q_operand(rng, M, K)
+    W, sW = q_weights(rng, 1, N, K)
+    _, acc, _ = oracle_mod.grouped_gemm(X, sX, W, sW, np.array([M], np.int32), 1, M, N, K, want_acc=True)
+    dense = oracle_mod.decode_operand(X, sX) @ oracle_mod.decode_operand(W[0], sW[0]).T
+    assert np.allclose(acc, dense, rtol=1e-12, atol=0)
+
+
+def test_grouped_gemm_points_and_rejects(oracle_mod):
+    rng = np.random.default_rng(33)
+    E, M, N, K = 3, 30, 5, 64
+    X, sX = q_operand(rng, M, K)
+    W, sW = q_weights(rng, E, N, K)
+    offs = np.array([7, 7, 26], np.int32)
+    full = oracle_mod.grouped_gemm(X, sX, W, sW, offs, E, M, N, K)
+    t = rng.integers(0, M, 40); n = rng.integers(0, N, 40)
+    pts = oracle_mod.grouped_gemm(X, sX, W, sW, offs, E, M, N, K, points=(t, n))
+    assert np.array_equal(pts, full[t, n])
+    with pytest.raises(ValueError):
+        oracle_mod.grouped_gemm(X, sX, W, sW, np.array([7, 5, 26], np.int32), E, M, N, K)  # decreasing
+    with pytest.raises(ValueError):
+        oracle_mod.grouped_gemm(X, sX, W, sW, np.array([7, 9, 31], np.int32), E, M, N, K)  # past M
