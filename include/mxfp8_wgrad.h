@@ -127,6 +127,42 @@ int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B
 int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, void* stream);
 
 /*
+ * MXFP8 grouped GEMM with ragged rows: the forward and data-gradient products
+ * of the same expert layer ("Group-GEMM in XLA", Part 1, the non-contracting
+ * ragged dot; the weight gradient above is its contracting form). The rows of
+ * X are cut into E contiguous groups by offs, and every row t of group g
+ * multiplies the weights of expert g:
+ *
+ *   out[t][n] = bf16_rne( sum_k x(t,k) w(g,n,k) ),
+ *   x(t,k) = e4m3(X[t][k]) * 2^(sX[t][k/32] - 127),  w likewise from W[g][n][k],
+ *
+ * accumulated in fp32 on the tensor cores, every output tile owned by one CTA
+ * pair (bit-reproducible). Forward: X = activations [M][K], W = expert weights
+ * [E][N][K] (output features x input features). Data gradient: X = dY [M][N'],
+ * W = the weights transposed per expert [E][K'][N'], both quantised along the
+ * contracted axis.
+ *
+ *   X    [M][K]      E4M3 bytes, 16-byte aligned
+ *   sX   [M][K/32]   E8M0 bytes
+ *   W    [E][N][K]   E4M3 bytes, 16-byte aligned
+ *   sW   [E][N][K/32] E8M0 bytes
+ *   offs [E]         int32 inclusive group ends over the rows of X; any row
+ *                    boundaries (no 32-alignment needed: the scale blocks run
+ *                    along k). Preconditions as for mxfp8_wgrad_grouped
+ *                    (non-decreasing, <= M; clamped on the device and flagged
+ *                    with MXFP8_DEV_OFFS_* otherwise). Rows at or past
+ *                    offs[E-1] are written as +0.0.
+ *   E    1..MXFP8_MAX_EXPERTS;  M rows (>= 1);  N >= 1, N % 8 == 0;  K >= 32, K % 32 == 0
+ *   out  [M][N] bf16, 16-byte aligned; every element is written
+ *
+ * Scratch comes from the same per-(device, stream) cache as
+ * mxfp8_wgrad_grouped. The tile width follows mxfp8_wgrad_set_tile_rows
+ * (the 256-row side is always on the rows of X).
+ */
+int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, const uint8_t* sW,
+                       const int32_t* offs, int E, int64_t M, int N, int K, uint16_t* out, void* stream);
+
+/*
  * Fused quantise-and-transpose from token-major bf16 (the layout in which the
  * forward and backward passes produce dY and X): x [M][R] bf16 (bit patterns,
  * 2-byte aligned) becomes q [R][M] E4M3 with the token axis contiguous

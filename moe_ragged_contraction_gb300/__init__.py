@@ -10,6 +10,7 @@ The Python API below is a thin ctypes binding: argument marshalling only.
 from ._lib import (  # noqa: F401
     Mxfp8Error,
     device_status,
+    grouped_gemm,
     lib_path,
     load,
     quantize_tokenwise,

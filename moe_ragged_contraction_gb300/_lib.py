@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
         lib.mxfp8_wgrad_grouped_ws.restype = I
         lib.mxfp8_quantize_tokenwise.argtypes = [P, I, L, P, P, P]
         lib.mxfp8_quantize_tokenwise.restype = I
+        lib.mxfp8_grouped_gemm.argtypes = [P, P, P, P, P, I, L, I, I, P, P]
+        lib.mxfp8_grouped_gemm.restype = I
         lib.mxfp8_quantize_transpose_bf16.argtypes = [P, L, I, P, P, P]
         lib.mxfp8_quantize_transpose_bf16.restype = I
         lib.mxfp8_last_error.argtypes = []
@@ -141,6 +143,33 @@ def wgrad_grouped(A, sA, B, sB, offs, out=None, workspace=None, stream=None):
         rc = lib.mxfp8_wgrad_grouped_ws(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offs), E, N, K, M,
                                         _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     check(rc)
+    return out
+
+
+def grouped_gemm(X, sX, W, sW, offs, out=None, stream=None):
+    """Grouped GEMM with ragged rows (see include/mxfp8_wgrad.h):
+    out[t] = x[t] . W[g(t)]^T for the rows t of group g.
+
+    X: uint8 [M, K] (E4M3), sX: uint8 [M, K/32], W: uint8 [E, N, K],
+    sW: uint8 [E, N, K/32], offs: int32 [E] inclusive group ends (device).
+    Returns (or fills) ``out``: bf16 [M, N].
+    """
+    import torch
+
+    for t, dt, nm in ((X, torch.uint8, "X"), (sX, torch.uint8, "sX"), (W, torch.uint8, "W"),
+                      (sW, torch.uint8, "sW"), (offs, torch.int32, "offs")):
+        _expect(t, dt, nm)
+    M, K = X.shape
+    E, N, K2 = W.shape
+    if K2 != K or tuple(sX.shape) != (M, K // 32) or tuple(sW.shape) != (E, N, K // 32) or offs.numel() != E:
+        raise ValueError("inconsistent operand / scale / offset shapes")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _expect(out, torch.bfloat16, "out")
+    if tuple(out.shape) != (M, N):
+        raise ValueError(f"out must be [{M}, {N}]")
+    check(load().mxfp8_grouped_gemm(_ptr(X), _ptr(sX), _ptr(W), _ptr(sW), _ptr(offs), E, M, N, K, _ptr(out),
+                                    _stream(stream)))
     return out
 
 

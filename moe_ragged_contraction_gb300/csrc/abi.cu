@@ -94,6 +94,25 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int rows, int64_t M,
     return MXFP8_OK;
 }
 
+// E4M3 operand [depth][rows][row_len] (row_len contiguous) -> 3-D boxes of
+// box_rows rows x 128 elements x 1, 128-byte swizzle; out-of-range rows and
+// columns read as zero (rows past `rows` never reach the next depth slice).
+int make_operand_map3(CUtensorMap* map, const uint8_t* base, int64_t row_len, int rows, int depth, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encoder(&enc);
+    if (rc) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_len), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(depth)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_len), static_cast<cuuint64_t>(row_len) * rows};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(mxw::BK), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MXFP8_ECUDA, "cuTensorMapEncodeTiled (3-D) failed (CUresult %d)", static_cast<int>(r));
+    return MXFP8_OK;
+}
+
 // Scale-factor workspace viewed as u32 [blocks][128] (one 512-byte block per
 // row); boxes of box_blocks whole blocks, no swizzle.
 int make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t blocks, int box_blocks) {
@@ -264,9 +283,9 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     const int n_rows = tc.kn ? N : K;
     rc = make_operand_map(&maps[0], m_op, tc.kn ? K : N, M, mxw::BM);
     if (rc) return rc;
-    rc = make_operand_map(&maps[1], n_op, n_rows, M, tc.n1 / 2);
+    rc = make_operand_map3(&maps[1], n_op, M, n_rows, 1, tc.n1 / 2);
     if (rc) return rc;
-    rc = make_operand_map(&maps[2], n_op, n_rows, M, tc.n2 ? tc.n2 / 2 : tc.n1 / 2);
+    rc = make_operand_map3(&maps[2], n_op, M, n_rows, 1, tc.n2 ? tc.n2 / 2 : tc.n1 / 2);
     if (rc) return rc;
     rc = make_sf_map(&maps[3], static_cast<uint8_t*>(ws) + lay.sfm_off, static_cast<int64_t>(tc.tiles_m) * lay.ts_max * 2, 1);
     if (rc) return rc;
@@ -350,6 +369,62 @@ int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8
     if (rc) return rc;
     cudaError_t e = mxw::launch_quantize(x, R, M, q, s, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "quantize kernel");
+    return MXFP8_OK;
+}
+
+int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, const uint8_t* sW,
+                       const int32_t* offs, int E, int64_t M, int N, int K, uint16_t* out, void* stream) {
+    if (E < 1 || E > MXFP8_MAX_EXPERTS) return fail(MXFP8_EINVAL, "E=%d out of range [1, %d]", E, MXFP8_MAX_EXPERTS);
+    if (M < 1 || M > (int64_t(1) << 31) - 1) return fail(MXFP8_EINVAL, "M=%lld out of range", (long long)M);
+    if (N < 1) return fail(MXFP8_EINVAL, "N=%d must be >= 1", N);
+    if (K < 32 || (K % 32) != 0) return fail(MXFP8_EINVAL, "K=%d must be a positive multiple of 32", K);
+    if (!X || !sX || !W || !sW || !offs || !out) return fail(MXFP8_EINVAL, "null pointer argument");
+    if (!aligned16(X) || !aligned16(W) || !aligned16(out))
+        return fail(MXFP8_EALIGN, "X, W and out must be 16-byte aligned");
+    if ((N % 8) != 0) return fail(MXFP8_EALIGN, "N=%d must be a multiple of 8 (16-byte output rows)", N);
+    mxw::TileConfig tc;
+    mxw::GemmLayout lay;
+    if (!mxw::choose_gemm_tiles(N, K, E, M, tile_rows_setting(), &tc) || !mxw::gemm_layout(E, N, K, M, tc, &lay))
+        return fail(MXFP8_EINVAL, "unsupported sizes");
+    int dev;
+    DeviceInfo info;
+    int rc = current_device(&dev, &info);
+    if (rc) return rc;
+    cudaEvent_t evb = g_ev_before, eva = g_ev_after;
+    g_ev_before = g_ev_after = nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    rc = cached_workspace(dev, st, lay.total, &ws);
+    if (rc) return rc;
+    // X: 256-row tiles, 128 rows per CTA; W as [E][N][K]: per CTA n1/2 rows for the
+    // first MMA and n2/2 for the second
+    CUtensorMap maps[5];
+    rc = make_operand_map(&maps[0], X, static_cast<int>(M), K, mxw::BM);
+    if (rc) return rc;
+    rc = make_operand_map3(&maps[1], W, K, N, E, tc.n1 / 2);
+    if (rc) return rc;
+    rc = make_operand_map3(&maps[2], W, K, N, E, tc.n2 ? tc.n2 / 2 : tc.n1 / 2);
+    if (rc) return rc;
+    rc = make_sf_map(&maps[3], static_cast<uint8_t*>(ws) + lay.sfm_off,
+                     static_cast<int64_t>(lay.mtiles_max) * lay.ksteps * 2, 1);
+    if (rc) return rc;
+    rc = make_sf_map(&maps[4], static_cast<uint8_t*>(ws) + lay.sfn_off,
+                     static_cast<int64_t>(E) * tc.tiles_n * lay.ksteps * tc.nblk_n, tc.nblk_n);
+    if (rc) return rc;
+    mxw::GemmArgs a;
+    a.X = X; a.sX = sX; a.W = W; a.sW = sW; a.offs = offs;
+    a.E = E; a.N = N; a.K = K; a.M = M; a.out = out;
+    a.ws = static_cast<uint8_t*>(ws);
+    a.lay = lay;
+    a.dev = dev;
+    a.num_sms = info.sms;
+    a.wait_limit_ns = wait_limit_ns();
+    a.stream = st;
+    a.ev_before = evb;
+    a.ev_after = eva;
+    const char* what = "";
+    cudaError_t e = mxw::launch_gemm(a, maps, &what);
+    if (e != cudaSuccess) return fail_cuda(e, what);
     return MXFP8_OK;
 }
 

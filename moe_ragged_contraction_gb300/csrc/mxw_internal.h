@@ -78,6 +78,38 @@ struct WgradArgs {
 // blocks). Returns a cudaError_t; `what` names the step.
 cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what);
 
+// Grouped GEMM (non-contracting ragged dot): out[t][n] = sum_k x(t,k) w(g,n,k)
+// for the rows t of group g; X [M][K], W [E][N][K] E4M3 with scales along k.
+// Tiles: 256 rows of X (a row tile never crosses a group) by tn rows of W[g].
+// Workspace: the plan (row-tile table), then the row tiles' scale-factor
+// blocks [mtiles_max][ksteps][2][512 B], then the weights' [E * tiles_n][ksteps][nblk_n][512 B].
+struct GemmLayout {
+    size_t plan_off, sfm_off, sfn_off, total;
+    int mtiles_max, ksteps;  // row tiles over every routing: ceil(M / 256) + E
+    TileConfig tc;
+};
+
+bool choose_gemm_tiles(int N, int K, int E, int64_t M, int force_tn, TileConfig* tc);
+bool gemm_layout(int E, int N, int K, int64_t M, const TileConfig& tc, GemmLayout* out);
+
+struct GemmArgs {
+    const uint8_t *X, *sX, *W, *sW;
+    const int32_t* offs;
+    int E, N, K;
+    int64_t M;
+    uint16_t* out;
+    uint8_t* ws;
+    GemmLayout lay;
+    int dev, num_sms;
+    uint64_t wait_limit_ns;
+    cudaStream_t stream;
+    cudaEvent_t ev_before, ev_after;
+};
+
+// maps: X (boxes of BM rows x BK), W as 3-D [E][N][K] (boxes of n1/2 and n2/2
+// rows), and the scale-factor blocks as u32 [blocks][128] (boxes of 1 and nblk_n).
+cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap* maps, const char** what);
+
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream);
 cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s,
                                       cudaStream_t stream);

@@ -250,6 +250,188 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     griddep_launch_dependents();
 }
 
+// ============================================================== grouped GEMM prep
+
+// Plan and scale re-layout of the grouped GEMM (the non-contracting ragged
+// dot: "Group-GEMM in XLA", Part 1; the forward and data-gradient products of
+// the expert layer): rows [offs[g-1], offs[g]) of X multiply W[g]. Every
+// block rebuilds the per-expert row runs from offs (clamped into [0, M],
+// non-decreasing) and their 256-row tiles; block 0 writes the plan: [0] items
+// (row tiles x N-side tiles), [1] E, [2] row tiles, then one int4 per row
+// tile (expert, first row, end of the expert's rows, 0). Then the blocks
+// gather scale-factor blocks for (row tile, half) and (expert, N-side tile,
+// 128-row block), one K-step each, and zero the output rows past the last
+// group.
+struct GemmPrepArgs {
+    const int32_t* offs;
+    const uint8_t *sX, *sW;    // [M][K/32], [E][N][K/32]
+    uint8_t *sfm, *sfn;        // [row tiles][ksteps][2][512], [E * tiles_n][ksteps][nblk][512]
+    int32_t* plan;
+    uint16_t* out;             // [M][N]
+    int E, N, K, ksteps, tn, tiles_n, nblk, mtiles_max;
+    long long M;
+};
+
+__global__ void __launch_bounds__(PREP_THREADS) gemm_prep(const GemmPrepArgs a) {
+    extern __shared__ int prep_smem[];
+    int* s_start = prep_smem;        // [E]
+    int* s_end = s_start + a.E;      // [E]
+    int* s_mtb = s_end + a.E;        // [E + 1]: first row tile of each expert, then the total
+    __shared__ int s_flags;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned full = 0xffffffffu;
+    const int E = a.E;
+    const long long M = a.M;
+
+    for (int g = threadIdx.x; g < E; g += PREP_THREADS) s_end[g] = a.offs[g];
+    __syncthreads();
+    if (warp == 0) {
+        long long carry_end = 0;
+        int carry_tiles = 0, flags = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int g = base + lane;
+            long long o = 0;
+            if (g < E) {
+                o = s_end[g];
+                if (o < 0) { o = 0; flags |= MXFP8_DEV_OFFS_RANGE; }
+                if (o > M) { o = M; flags |= MXFP8_DEV_OFFS_RANGE; }
+            }
+            long long m = o;  // inclusive running max -> clamped non-decreasing ends
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const long long t = __shfl_up_sync(full, m, d);
+                if (lane >= d) m = max(m, t);
+            }
+            const long long end = max(m, carry_end);
+            long long start = __shfl_up_sync(full, end, 1);
+            if (lane == 0) start = carry_end;
+            if (g < E && o < start) flags |= MXFP8_DEV_OFFS_UNSORTED;
+            const int nt = static_cast<int>((end - start + 2 * BM - 1) / (2 * BM));
+            int incl = nt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int t = __shfl_up_sync(full, incl, d);
+                if (lane >= d) incl += t;
+            }
+            __syncwarp();
+            if (g < E) {
+                s_start[g] = static_cast<int>(start);
+                s_end[g] = static_cast<int>(end);
+                s_mtb[g] = carry_tiles + incl - nt;
+            }
+            carry_end = __shfl_sync(full, end, 31);
+            carry_tiles += __shfl_sync(full, incl, 31);
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) flags |= __shfl_xor_sync(full, flags, d);
+        if (lane == 0) {
+            s_mtb[E] = carry_tiles;
+            s_flags = flags;
+        }
+    }
+    __syncthreads();
+    const int mtiles = s_mtb[E];
+
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) {
+            a.plan[0] = mtiles * a.tiles_n;
+            a.plan[1] = E;
+            a.plan[2] = mtiles;
+            if (s_flags) atomicOr(&g_device_status, s_flags);
+        }
+        int4* ent = reinterpret_cast<int4*>(a.plan + PLAN_HDR);
+        for (int g = threadIdx.x; g < E; g += PREP_THREADS)
+            for (int j = 0, mt = s_mtb[g]; mt < s_mtb[g + 1]; ++j, ++mt)
+                ent[mt] = make_int4(g, s_start[g] + 2 * BM * j, s_end[g], 0);
+    }
+
+    // scale-factor gather: tasks (128-row block, 32 consecutive K-steps), the
+    // row tiles' halves first, then the (expert, N-side tile) blocks
+    uint32_t* tile = reinterpret_cast<uint32_t*>(s_mtb + E + 1);  // [PREP_ROWS][PREP_TILE_STEPS + 1]
+    const int nchunks = (a.ksteps + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS;
+    const int mblocks = 2 * mtiles;
+    const long long nblk_total = static_cast<long long>(mblocks) + static_cast<long long>(E) * a.tiles_n * a.nblk;
+    const long long ntasks = nblk_total * nchunks;
+    const long long sK = a.K / 32;
+    for (long long task = blockIdx.x; task < ntasks; task += gridDim.x) {
+        const long long hb = task / nchunks;
+        const int s0 = static_cast<int>(task - hb * nchunks) * PREP_TILE_STEPS;
+        const bool mside = hb < mblocks;
+        const uint8_t* plane;
+        uint8_t* dst0;  // block of K-step 0; consecutive K-steps `stride` bytes apart
+        size_t stride, plane_bytes;
+        long long row0;
+        int rows_valid;  // rows of this 128-row block that exist
+        if (mside) {
+            const int mt = static_cast<int>(hb >> 1), h = static_cast<int>(hb & 1);
+            int lo = 0, hi = E;  // expert of row tile mt: the last g with s_mtb[g] <= mt
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_mtb[mid] <= mt) lo = mid; else hi = mid;
+            }
+            row0 = static_cast<long long>(s_start[lo]) + 2LL * BM * (mt - s_mtb[lo]) + PREP_ROWS * h;
+            const long long left = s_end[lo] - row0;
+            rows_valid = static_cast<int>(left < 0 ? 0 : (left > PREP_ROWS ? PREP_ROWS : left));
+            plane = a.sX;
+            plane_bytes = static_cast<size_t>(M) * sK;
+            dst0 = a.sfm + (static_cast<size_t>(mt) * a.ksteps * 2 + h) * SF_ATOM;
+            stride = 2 * SF_ATOM;
+        } else {
+            const long long nb = hb - mblocks;  // (g * tiles_n + tn) * nblk + h
+            const int h = static_cast<int>(nb % a.nblk);
+            const long long gt = nb / a.nblk;
+            const int g = static_cast<int>(gt / a.tiles_n), tn = static_cast<int>(gt % a.tiles_n);
+            const int in_tile0 = PREP_ROWS * h;
+            row0 = static_cast<long long>(tn) * a.tn + in_tile0;
+            const long long left = min(static_cast<long long>(a.tn - in_tile0), static_cast<long long>(a.N) - row0);
+            rows_valid = static_cast<int>(left < 0 ? 0 : (left > PREP_ROWS ? PREP_ROWS : left));
+            plane = a.sW + static_cast<size_t>(g) * a.N * sK;
+            plane_bytes = static_cast<size_t>(a.N) * sK;
+            dst0 = a.sfn + (static_cast<size_t>(gt) * a.ksteps * a.nblk + h) * SF_ATOM;
+            stride = static_cast<size_t>(a.nblk) * SF_ATOM;
+        }
+        const int s = s0 + lane;  // this lane's K-step
+        int nvalid = 0;
+        if (s < a.ksteps) {
+            const int left = (a.K - s * BK + 31) >> 5;
+            nvalid = left < 4 ? left : 4;
+        }
+        const uint32_t keep = nvalid >= 4 ? 0xffffffffu : ((1u << (8 * nvalid)) - 1u);
+        constexpr int ROWS_PER_WARP = PREP_ROWS / (PREP_THREADS / 32);
+        uint32_t wv[ROWS_PER_WARP];
+#pragma unroll
+        for (int i = 0; i < ROWS_PER_WARP; ++i) {
+            const int r = warp + i * (PREP_THREADS / 32);
+            const bool ok = nvalid > 0 && r < rows_valid;
+            wv[i] = ok ? (load_scale4(plane, static_cast<size_t>(row0 + r) * sK + 4 * s, plane_bytes) & keep) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < ROWS_PER_WARP; ++i)
+            tile[(warp + i * (PREP_THREADS / 32)) * (PREP_TILE_STEPS + 1) + lane] = wv[i];
+        __syncthreads();
+        for (int j = warp; j < PREP_TILE_STEPS; j += PREP_THREADS / 32) {
+            if (s0 + j >= a.ksteps) continue;
+            uint4 o;
+            o.x = tile[(lane + 0) * (PREP_TILE_STEPS + 1) + j];
+            o.y = tile[(lane + 32) * (PREP_TILE_STEPS + 1) + j];
+            o.z = tile[(lane + 64) * (PREP_TILE_STEPS + 1) + j];
+            o.w = tile[(lane + 96) * (PREP_TILE_STEPS + 1) + j];
+            reinterpret_cast<uint4*>(dst0 + static_cast<size_t>(s0 + j) * stride)[lane] = o;
+        }
+        __syncthreads();
+    }
+    // rows past the last group belong to no expert: exact zeros
+    {
+        const long long end_last = E > 0 ? s_end[E - 1] : 0;
+        const long long n_zero = (M - end_last) * a.N;  // N % 8 == 0: 16-byte runs
+        uint4* z = reinterpret_cast<uint4*>(a.out + end_last * a.N);
+        for (long long i = static_cast<long long>(blockIdx.x) * PREP_THREADS + threadIdx.x; i < n_zero / 8;
+             i += static_cast<long long>(gridDim.x) * PREP_THREADS)
+            z[i] = make_uint4(0, 0, 0, 0);
+    }
+    griddep_launch_dependents();
+}
+
 // ============================================================== main kernel
 
 // One CTA pair (a 2-CTA cluster) owns a 256 x TN output tile. CTA r of the
@@ -295,7 +477,11 @@ constexpr uint32_t IDESC_BASE = (1u << 23) | (static_cast<uint32_t>(PAIR_M >> 4)
 struct MainParams {
     const int32_t* plan;
     uint16_t* out;
-    int E, N, K;             // out[E][N][K]
+    int mode;                // 0: weight gradient (contraction over ragged token runs); 1: grouped GEMM (ragged rows)
+    int E, N, K;             // mode 0: out[E][N][K]; mode 1: out[M][N], K the contracted length
+    long long out_stride;    // elements between output rows (rows of the 256-row side)
+    int col_limit;           // valid output columns (columns of the tn side)
+    int ksteps;              // mode 1: K-steps of every tile
     int ts_max;
     int tiles_m, tiles_n;    // pair tiles along the M side (256 rows) and the N side (tn rows)
     int tn, n1, n2;          // N-side tile rows = n1 + n2 (the two MMA widths; n2 may be 0)
@@ -343,25 +529,57 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, unsig
 }
 
 struct Item {
-    int g, tm, tn, start, len, nsteps, step_base;
+    int g, tm, tn;        // expert, M-side and N-side tile
+    int start, len;       // contraction: first coordinate and length
+    int nsteps;           // K-steps
+    int m0, m_end;        // M-side rows of the tile start at m0; rows at or past m_end are not stored
+    int sfm, sfn;         // scale-factor block rows of the tile's first K-step (M side: this CTA adds its rank)
+    int z;                // N-side tensor-map depth coordinate (the expert in the grouped GEMM)
+    long long orow0;      // output row of M-side row 0 (rows of the 256 side)
 };
 
-// Work item i (in longest-expert-first order, the tiles of one expert
-// consecutive, N-side tiles fastest) -> expert and pair tile.
-__device__ __forceinline__ Item load_item(const int32_t* __restrict__ plan, int E, int tiles_n, int nt_per_expert,
-                                          long long i) {
-    const int32_t* ex = plan + PLAN_HDR;
-    const int32_t* order = ex + 4 * E;
-    const int r = static_cast<int>(i / nt_per_expert);
-    const int t = static_cast<int>(i - static_cast<long long>(r) * nt_per_expert);
+// Work item i -> expert and pair tile.
+// Mode 0 (weight gradient): items in longest-expert-first order, the tiles of
+// one expert consecutive, N-side tiles fastest; plan entries per expert.
+// Mode 1 (grouped GEMM): item = (row tile, N-side tile), N-side fastest; the
+// plan holds one entry per row tile: (expert, first row, end of the expert's rows).
+__device__ __forceinline__ Item load_item(const MainParams& p, long long i) {
     Item it;
-    it.g = __ldg(order + r);
-    it.tm = t / tiles_n;
-    it.tn = t - it.tm * tiles_n;
-    it.start = __ldg(ex + 4 * it.g + 0);
-    it.len = __ldg(ex + 4 * it.g + 1);
-    it.nsteps = __ldg(ex + 4 * it.g + 2);
-    it.step_base = __ldg(ex + 4 * it.g + 3);
+    if (p.mode == 0) {
+        const int32_t* ex = p.plan + PLAN_HDR;
+        const int32_t* order = ex + 4 * p.E;
+        const int ntpe = p.tiles_m * p.tiles_n;
+        const int r = static_cast<int>(i / ntpe);
+        const int t = static_cast<int>(i - static_cast<long long>(r) * ntpe);
+        it.g = __ldg(order + r);
+        it.tm = t / p.tiles_n;
+        it.tn = t - it.tm * p.tiles_n;
+        it.start = __ldg(ex + 4 * it.g + 0);
+        it.len = __ldg(ex + 4 * it.g + 1);
+        it.nsteps = __ldg(ex + 4 * it.g + 2);
+        const int sb = __ldg(ex + 4 * it.g + 3);
+        it.m0 = it.tm * (2 * BM);
+        it.m_end = p.kn ? p.K : p.N;
+        it.sfm = (it.tm * p.ts_max + sb) * 2;
+        it.sfn = (it.tn * p.ts_max + sb) * p.nblk_n;
+        it.z = 0;
+        it.orow0 = static_cast<long long>(it.g) * p.N;
+    } else {
+        const int mt = static_cast<int>(i / p.tiles_n);
+        it.tn = static_cast<int>(i - static_cast<long long>(mt) * p.tiles_n);
+        const int4 e = __ldg(reinterpret_cast<const int4*>(p.plan + PLAN_HDR) + mt);
+        it.g = e.x;
+        it.tm = mt;
+        it.m0 = e.y;
+        it.m_end = e.z;
+        it.start = 0;
+        it.len = p.K;
+        it.nsteps = p.ksteps;
+        it.sfm = mt * p.ksteps * 2;
+        it.sfn = (it.g * p.tiles_n + it.tn) * p.ksteps * p.nblk_n;
+        it.z = it.g;
+        it.orow0 = 0;
+    }
     return it;
 }
 
@@ -387,23 +605,22 @@ __device__ __forceinline__ long long next_item(long long& pass, int G, int pair,
 // This pair's items in schedule order, the next item's plan entry loaded one
 // item ahead so that its global-memory latency overlaps the current item.
 struct ItemStream {
-    const int32_t* plan;
-    int E, tiles_n, nt_per_expert, G, pair;
+    const MainParams& p;
+    int G, pair;
     long long total, pass, i_next;
     Item it_next;
 
-    __device__ __forceinline__ ItemStream(const int32_t* plan_, int E_, int tiles_n_, int ntpe, int G_, int pair_,
-                                          long long total_)
-        : plan(plan_), E(E_), tiles_n(tiles_n_), nt_per_expert(ntpe), G(G_), pair(pair_), total(total_), pass(0) {
+    __device__ __forceinline__ ItemStream(const MainParams& p_, int G_, int pair_, long long total_)
+        : p(p_), G(G_), pair(pair_), total(total_), pass(0) {
         i_next = next_item(pass, G, pair, total);
-        if (i_next >= 0) it_next = load_item(plan, E, tiles_n, nt_per_expert, i_next);
+        if (i_next >= 0) it_next = load_item(p, i_next);
     }
 
     __device__ __forceinline__ bool next(Item& it) {
         if (i_next < 0) return false;
         it = it_next;
         i_next = next_item(pass, G, pair, total);
-        if (i_next >= 0) it_next = load_item(plan, E, tiles_n, nt_per_expert, i_next);
+        if (i_next >= 0) it_next = load_item(p, i_next);
         return true;
     }
 };
@@ -450,7 +667,7 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
     uint32_t c = 0;
     uint32_t st = 0, slot = 0, buf = 0, acc_phase = 0;  // accumulator buffer of the current tile and its use count parity
     bool live = true;
-    ItemStream items(p.plan, p.E, p.tiles_n, x.nt_per_expert, x.G, x.pair, x.total);
+    ItemStream items(p, x.G, x.pair, x.total);
     Item it;
     while (items.next(it)) {
         if (it.nsteps == 0) continue;
@@ -562,8 +779,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
     // everything below reads the plan and scale blocks of the preceding kernel
     griddep_wait();
 
+    // mode 1: the number of row tiles depends on the routing; the plan holds the item count
     const int nt_per_expert = p.tiles_m * p.tiles_n;
-    const long long total = static_cast<long long>(p.E) * nt_per_expert;
+    const long long total =
+        p.mode == 0 ? static_cast<long long>(p.E) * nt_per_expert : static_cast<long long>(__ldg(p.plan));
     const int G = gridDim.x / 2, pair = blockIdx.x / 2;
 
     if (warp == 0) {
@@ -577,14 +796,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             int st = 0;
             uint32_t ph = 0;
             bool ok = true;
-            ItemStream items(p.plan, p.E, p.tiles_n, nt_per_expert, G, pair, total);
+            ItemStream items(p, G, pair, total);
             Item it;
             while (ok && items.next(it)) {
-                const int m_row = it.tm * PAIR_M + static_cast<int>(rank) * BM;
+                const int m_row = it.m0 + static_cast<int>(rank) * BM;
                 const int n_row1 = it.tn * p.tn + static_cast<int>(rank) * h1;
                 const int n_row2 = it.tn * p.tn + p.n1 + static_cast<int>(rank) * h2;
-                const int sfm_row = (it.tm * p.ts_max + it.step_base) * 2 + static_cast<int>(rank);
-                const int sfn_row = (it.tn * p.ts_max + it.step_base) * p.nblk_n;
+                const int sfm_row = it.sfm + static_cast<int>(rank);
+                const int sfn_row = it.sfn;
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
                     // test hook: only the (over-declared) first fill is issued, so the
                     // stuck phase is never re-armed
@@ -595,8 +814,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                     const int x = it.start + s * BK;
                     const uint32_t b_dst = sbase + p.off_b + st * p.b_stage;
                     tma_load_2d_pair(sbase + st * A_STAGE, &tmM, fb, x, m_row);
-                    tma_load_2d_pair(b_dst, &tmN1, fb, x, n_row1);
-                    if (h2) tma_load_2d_pair(b_dst + h1 * BK, &tmN2, fb, x, n_row2);
+                    tma_load_3d_pair(b_dst, &tmN1, fb, x, n_row1, it.z);
+                    if (h2) tma_load_3d_pair(b_dst + h1 * BK, &tmN2, fb, x, n_row2, it.z);
                     tma_load_2d_pair(sbase + p.off_sfa + st * SF_ATOM, &tmSFM, fb, 0, sfm_row + 2 * s);
                     tma_load_2d_pair(sbase + p.off_sfb + st * sfb_stage, &tmSFN, fb, 0, sfn_row + p.nblk_n * s);
                     if (++st == S) { st = 0; ph ^= 1; }
@@ -638,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             uint32_t c = 0;
             bool live = true;
             const bool gate = p.sf_slots < S;
-            ItemStream items(p.plan, p.E, p.tiles_n, nt_per_expert, G, pair, total);
+            ItemStream items(p, G, pair, total);
             Item it;
             while (items.next(it)) {
                 for (int s = 0; s < it.nsteps; ++s, ++c) {
@@ -691,15 +910,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             for (int pass = 0; pass * G < total32; ++pass) {
                 const int i = (pass & 1) ? pass * G + (G - 1 - pair) : pass * G + pair;
                 if (i >= total32) continue;
-                const Item it = load_item(p.plan, p.E, p.tiles_n, nt_per_expert, i);
-                const int mrow = it.tm * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;  // this lane's M-side row
+                const Item it = load_item(p, i);
+                const int mrow = it.m0 + static_cast<int>(rank) * BM + q * 32 + lane;  // this lane's M-side row
                 const int ncol0 = it.tn * p.tn + h * ncols;                                      // first N-side row here
                 // NK: a lane owns output row mrow; KN: a lane owns output column
                 // mrow, and lane pairs share the column pair (k2, k2 + 1)
                 const int k2 = mrow & ~1;
-                const bool row_in = MODE == 2 ? (k2 < p.K) : (mrow < p.N);
+                const bool row_in = MODE == 2 ? (k2 < p.K) : (mrow < it.m_end);
                 uint16_t* obase = MODE == 2 ? p.out + static_cast<size_t>(it.g) * p.N * static_cast<size_t>(p.K) + k2
-                                       : p.out + (static_cast<size_t>(it.g) * p.N + mrow) * static_cast<size_t>(p.K) + ncol0;
+                                       : p.out + static_cast<size_t>(it.orow0 + mrow) * static_cast<size_t>(p.out_stride) + ncol0;
                 // Narrow one 32-column chunk (columns 32 j .. 32 j + 31 of this warp's
                 // half) to bf16 and store it. NK: 16-byte runs of the lane's row.
                 // KN: neighbouring lanes swap their (n, n+1) pairs so that the even
@@ -711,7 +930,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
 #pragma unroll
                         for (int c = 0; c < 32; c += 16) {
                             const int cc = 32 * j + c;
-                            if (row_in && cc < ncols && ncol0 + cc < p.K)
+                            if (row_in && cc < ncols && ncol0 + cc < p.col_limit)
                                 st_global_v8(obase + cc, pack_bf16x2(v[c + 0], v[c + 1]),
                                              pack_bf16x2(v[c + 2], v[c + 3]), pack_bf16x2(v[c + 4], v[c + 5]),
                                              pack_bf16x2(v[c + 6], v[c + 7]), pack_bf16x2(v[c + 8], v[c + 9]),
@@ -722,7 +941,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             const int cc = 32 * j + c;
-                            if (row_in && cc < ncols && ncol0 + cc < p.K)
+                            if (row_in && cc < ncols && ncol0 + cc < p.col_limit)
                                 *reinterpret_cast<uint4*>(obase + cc) =
                                     make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
                                                pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
@@ -908,6 +1127,10 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, b
     return best;
 }
 
+static cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& geo, long long items,
+                               const CUtensorMap* maps, int dev, int num_sms, cudaStream_t stream,
+                               cudaEvent_t ev_before, cudaEvent_t ev_after);
+
 }  // namespace
 
 bool choose_tiles(int N, int K, int E, int64_t M, int force, int force_tn, TileConfig* tc) {
@@ -1007,32 +1230,50 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     }
 
     *what = "main contraction kernel";
+    MainParams mp;
+    mp.plan = plan;
+    mp.out = a.out;
+    mp.mode = 0;
+    mp.out_stride = a.K;
+    mp.col_limit = a.K;
+    mp.ksteps = 0;
+    mp.E = a.E;
+    mp.N = a.N;
+    mp.K = a.K;
+    mp.ts_max = L.ts_max;
+    mp.tiles_m = tc.tiles_m;
+    mp.wide_stores = (!tc.kn && tc.tn % 32 == 0 && a.K % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;
+    mp.wait_ns = a.wait_limit_ns;
+    mp.stall_first_stage = a.stall_first_stage;
+    const long long total = static_cast<long long>(a.E) * tc.tiles_m * tc.tiles_n;
+    return launch_main(mp, tc, geo, total, maps, a.dev, a.num_sms, a.stream, a.ev_before, a.ev_after);
+}
+
+// The persistent CTA-pair kernel for either mode, as a programmatic
+// dependent of the prep kernel just enqueued. `items` bounds the work items
+// (the grid is the smaller of it and the resident pairs).
+namespace {
+cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& geo, long long items,
+                        const CUtensorMap* maps, int dev, int num_sms, cudaStream_t stream, cudaEvent_t ev_before,
+                        cudaEvent_t ev_after) {
     // per device: the shared-memory opt-in and the number of CTA pairs that
     // can be resident at once (the persistent grid; one CTA per SM whatever
     // the tile, as the register file holds only one)
     static int max_pairs[64] = {};
-    if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
-    if (max_pairs[a.dev] == 0) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (max_pairs[dev] == 0) {
         cudaError_t e = cudaFuncSetAttribute(wgrad_main, cudaFuncAttributeMaxDynamicSharedMemorySize, MAIN_SMEM_MAX);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t q = {};
-        q.gridDim = dim3(2 * (a.num_sms / 2));
+        q.gridDim = dim3(2 * (num_sms / 2));
         q.blockDim = dim3(MAIN_THREADS);
         q.dynamicSmemBytes = MAIN_SMEM_MAX;
         int clusters = 0;
         e = cudaOccupancyMaxActiveClusters(&clusters, wgrad_main, &q);
         if (e != cudaSuccess) return e;
         if (clusters < 1) return cudaErrorInvalidConfiguration;
-        max_pairs[a.dev] = clusters;
+        max_pairs[dev] = clusters;
     }
-    MainParams mp;
-    mp.plan = plan;
-    mp.out = a.out;
-    mp.E = a.E;
-    mp.N = a.N;
-    mp.K = a.K;
-    mp.ts_max = L.ts_max;
-    mp.tiles_m = tc.tiles_m;
     mp.tiles_n = tc.tiles_n;
     mp.tn = tc.tn;
     mp.n1 = tc.n1;
@@ -1042,19 +1283,15 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     mp.stages = geo.stages;
     mp.sf_slots = geo.sf_slots;
     mp.acc_bufs = geo.acc_bufs;
-    mp.wide_stores = (!tc.kn && tc.tn % 32 == 0 && a.K % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;
     mp.sf_col0 = geo.sf_col0;
     mp.off_b = geo.off_b;
     mp.off_sfa = geo.off_sfa;
     mp.off_sfb = geo.off_sfb;
     mp.off_bar = geo.off_bar;
     mp.b_stage = geo.b_stage;
-    mp.wait_ns = a.wait_limit_ns;
-    mp.stall_first_stage = a.stall_first_stage;
-    const long long total = static_cast<long long>(a.E) * tc.tiles_m * tc.tiles_n;
-    const int pairs = static_cast<int>(total < max_pairs[a.dev] ? total : max_pairs[a.dev]);
-    if (a.ev_before) {
-        cudaError_t e = cudaEventRecord(a.ev_before, a.stream);
+    const int pairs = static_cast<int>(items < max_pairs[dev] ? (items > 0 ? items : 1) : max_pairs[dev]);
+    if (ev_before) {
+        cudaError_t e = cudaEventRecord(ev_before, stream);
         if (e != cudaSuccess) return e;
     }
     // programmatic dependent launch: the prologue (barriers, TMEM allocation,
@@ -1064,7 +1301,7 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(MAIN_THREADS);
     cfg.dynamicSmemBytes = geo.smem_bytes;
-    cfg.stream = a.stream;
+    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1074,11 +1311,114 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (a.ev_after) {
-        e = cudaEventRecord(a.ev_after, a.stream);
+    if (ev_after) {
+        e = cudaEventRecord(ev_after, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------- grouped GEMM host side
+
+bool choose_gemm_tiles(int N, int K, int E, int64_t M, int force_tn, TileConfig* tc) {
+    if (N < 1 || K < 32 || E < 1 || M < 1) return false;
+    const double ksteps = static_cast<double>((K + BK - 1) / BK);
+    double cost;
+    *tc = best_of(0, static_cast<int>(M < (int64_t(1) << 30) ? M : (int64_t(1) << 30)), N, ksteps, force_tn,
+                  N % 16 == 0, &cost);
+    return cost >= 0;
+}
+
+bool gemm_layout(int E, int N, int K, int64_t M, const TileConfig& tc, GemmLayout* L) {
+    if (E < 1 || E > MXFP8_MAX_EXPERTS || N < 1 || K < 32 || (K % 32) != 0 || M < 1) return false;
+    if (M > (int64_t(1) << 31) - 1) return false;
+    const int64_t mtiles = (M + 2 * BM - 1) / (2 * BM) + E;
+    const int64_t ksteps = (K + BK - 1) / BK;
+    if (mtiles * tc.tiles_n > (int64_t(1) << 31) - 1) return false;
+    const int64_t rows_m = mtiles * ksteps * 2;
+    const int64_t rows_n = static_cast<int64_t>(E) * tc.tiles_n * ksteps * tc.nblk_n;
+    if (rows_m > (int64_t(1) << 31) - 1 || rows_n > (int64_t(1) << 31) - 1) return false;
+    L->mtiles_max = static_cast<int>(mtiles);
+    L->ksteps = static_cast<int>(ksteps);
+    L->tc = tc;
+    const size_t plan_bytes = sizeof(int32_t) * (PLAN_HDR + 4 * static_cast<size_t>(mtiles));
+    L->plan_off = 0;
+    L->sfm_off = (plan_bytes + 1023) & ~size_t(1023);
+    L->sfn_off = L->sfm_off + static_cast<size_t>(rows_m) * SF_ATOM;
+    L->total = L->sfn_off + static_cast<size_t>(rows_n) * SF_ATOM;
+    return true;
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap* maps, const char** what) {
+    const GemmLayout& L = a.lay;
+    const TileConfig& tc = L.tc;
+    int32_t* plan = reinterpret_cast<int32_t*>(a.ws + L.plan_off);
+    Geometry geo;
+    *what = "tile geometry";
+    if (!geometry(tc.tn, &geo)) return cudaErrorInvalidConfiguration;
+
+    *what = "grouped GEMM plan / scale re-layout kernel";
+    {
+        GemmPrepArgs pa;
+        pa.offs = a.offs;
+        pa.sX = a.sX;
+        pa.sW = a.sW;
+        pa.sfm = a.ws + L.sfm_off;
+        pa.sfn = a.ws + L.sfn_off;
+        pa.plan = plan;
+        pa.out = a.out;
+        pa.E = a.E;
+        pa.N = a.N;
+        pa.K = a.K;
+        pa.ksteps = L.ksteps;
+        pa.tn = tc.tn;
+        pa.tiles_n = tc.tiles_n;
+        pa.nblk = tc.nblk_n;
+        pa.mtiles_max = L.mtiles_max;
+        pa.M = a.M;
+        const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
+                          sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
+        static bool attr_set[64] = {};
+        if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
+        if (!attr_set[a.dev]) {
+            cudaError_t e0 = cudaFuncSetAttribute(gemm_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+            if (e0 != cudaSuccess) return e0;
+            attr_set[a.dev] = true;
+        }
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_prep, PREP_THREADS, sm);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+        const long long chunks = (L.ksteps + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS;
+        const long long tasks = (2LL * L.mtiles_max + static_cast<long long>(a.E) * tc.tiles_n * tc.nblk_n) * chunks;
+        long long blocks = tasks;
+        if (blocks > static_cast<long long>(per_sm) * a.num_sms) blocks = static_cast<long long>(per_sm) * a.num_sms;
+        if (blocks < 1) blocks = 1;
+        gemm_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(pa);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    *what = "grouped GEMM main kernel";
+    MainParams mp;
+    mp.plan = plan;
+    mp.out = a.out;
+    mp.mode = 1;
+    mp.out_stride = a.N;
+    mp.col_limit = a.N;
+    mp.ksteps = L.ksteps;
+    mp.E = a.E;
+    mp.N = a.N;
+    mp.K = a.K;
+    mp.ts_max = 0;
+    mp.tiles_m = 0;
+    mp.wide_stores = (tc.tn % 32 == 0 && a.N % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;
+    mp.wait_ns = a.wait_limit_ns;
+    mp.stall_first_stage = 0;
+    const long long items = static_cast<long long>(L.mtiles_max) * tc.tiles_n;
+    return launch_main(mp, tc, geo, items, maps, a.dev, a.num_sms, a.stream, a.ev_before, a.ev_after);
 }
 
 cudaError_t set_suspend_hint(uint32_t ns) { return cudaMemcpyToSymbol(g_suspend_ns, &ns, sizeof(ns)); }
