@@ -521,6 +521,119 @@ def bench_quantizer(args):
             "gpu_launches": 2 * K}
 
 
+# ------------------------------------------------------------------ grouped GEMM (forward / data gradient)
+
+def _rowwise_mxfp8(rows: int, cols: int, seed: int, stream: int, dist: str, device):
+    """Seeded fp32 [rows, cols] generated and quantised on the GPU in row
+    chunks, 32-element blocks along the last axis (input building; not timed)."""
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+    s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=device)
+    step = max(1, (1 << 30) // (4 * cols))
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        x = I.device_operand(r1 - r0, cols, seed * 7919 + r0, stream, dist, device=device)
+        mx.quantize_tokenwise(x, q[r0:r1], s[r0:r1])
+        del x
+    return q, s
+
+
+def bench_gemm(args):
+    """Opt-in line: the same expert layer's other two products, as grouped
+    GEMMs with ragged rows on the workload's routing: forward Y = X W[g]^T
+    (X [M, K], W [E, N, K], contracting K) and data gradient dX = dY W[g]
+    (dY [M, N], W stored [E, K, N], contracting N). One step = both calls."""
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    mx.build()
+    mx.load()
+    w = I.WORKLOADS[args.config]
+    E, N, K, M = w.E, w.N, w.K, w.M
+    X, sX = _rowwise_mxfp8(M, K, w.seed, 20, w.dist, device)
+    dY, sdY = _rowwise_mxfp8(M, N, w.seed, 21, w.dist, device)
+    W, sW = _rowwise_mxfp8(E * N, K, w.seed, 22, "normal", device)
+    Wt, sWt = _rowwise_mxfp8(E * K, N, w.seed, 23, "normal", device)
+    W, sW = W.view(E, N, K), sW.view(E, N, K // 32)
+    Wt, sWt = Wt.view(E, K, N), sWt.view(E, K, N // 32)
+    offs = torch.from_numpy(I.offsets(I.group_sizes(args.config))).to(device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(pairs=None):
+        if pairs is not None:
+            mx.set_timing_events(*pairs[0])
+        mx.grouped_gemm(X, sX, W, sW, offs, out=y)
+        if pairs is not None:
+            mx.set_timing_events(*pairs[1])
+        mx.grouped_gemm(dY, sdY, Wt, sWt, offs, out=dx)
+
+    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(device).uuid))
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    S = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(S)]
+    evm = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+           for _ in range(S)]
+    for pr in evm:
+        for a, b in pr:
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    hold_gpu(2 * S)
+    for i in range(S):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    hold_gpu(2 * S)
+    for i in range(S):
+        flush.zero_()
+        step(pairs=evm[i])
+    torch.cuda.synchronize()
+    fwd_ms = float(np.mean([p[0][0].elapsed_time(p[0][1]) for p in evm]))
+    dgr_ms = float(np.mean([p[1][0].elapsed_time(p[1][1]) for p in evm]))
+    clocks = sampler.stop()
+    assert mx.device_status(clear=True) == 0, "device flagged an error during the benchmark"
+    routed = int(offs[-1].item()) if E else 0
+    flop_call = 2.0 * routed * N * K
+    peak, peak_src, _ = mxfp8_peak()
+    achieved = 2 * flop_call / ((fwd_ms + dgr_ms) * 1e-3) / 1e12
+    value = 2 * flop_call / (ms * 1e-3) / 1e12
+    return {"metric": "TFLOP/s (2*N*K*sum(M_g) per call) MXFP8 grouped GEMM with ragged rows, forward + data gradient",
+            "value": value, "unit": "TFLOP/s", "ms_per_step": ms, "steps": S, "warmup": args.warmup,
+            "higher_is_better": True,
+            "dtype": "mxfp8_e4m3 (e8m0 block-32 scales), fp32 accumulate, bf16 out",
+            "data": "synthetic (seeded routing, operands quantised on the GPU)",
+            "config": {"workload": args.config, "E": E, "N": N, "K": K, "M": M, "routing": w.description,
+                       "forward": f"[{M},{K}] x [{E},{N},{K}]^T -> [{M},{N}]",
+                       "dgrad": f"[{M},{N}] x [{E},{K},{N}]^T -> [{M},{K}]",
+                       "l2": "flushed (256 MiB write) before every timed step"},
+            "pct_of_mxfp8_peak": 100.0 * value / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": peak_src, "kernel": "wgrad_main (row-tile mode)",
+                         "algorithmic_flop_per_launch": flop_call, "traffic": None,
+                         "forward_main_ms": fwd_ms, "dgrad_main_ms": dgr_ms,
+                         "forward_tflops": flop_call / (fwd_ms * 1e-3) / 1e12,
+                         "dgrad_tflops": flop_call / (dgr_ms * 1e-3) / 1e12},
+            "gpu_launches": 4 * S,
+            "clocks": clocks}
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 
 def _host_inputs(name: str):
@@ -592,6 +705,8 @@ def main():
                     help="print a context line with vendor BF16 grouped / dense MXFP8 GEMM timings instead")
     ap.add_argument("--quantizer", action="store_true",
                     help="print a line for the fused bf16 quantise-and-transpose of the workload's operands instead")
+    ap.add_argument("--gemm", action="store_true",
+                    help="print a line for the layer's forward and data-gradient grouped GEMMs (ragged rows) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -599,6 +714,8 @@ def main():
         res = bench_comparators(args)
     elif args.quantizer:
         res = bench_quantizer(args)
+    elif args.gemm:
+        res = bench_gemm(args)
     else:
         res = bench_reference_arm(args) if args.impl == "reference" else bench_gpu(args)
     if res is not None:

@@ -163,6 +163,15 @@ int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, co
                        const int32_t* offs, int E, int64_t M, int N, int K, uint16_t* out, void* stream);
 
 /*
+ * Tiling mxfp8_grouped_gemm would use for these sizes under the current
+ * settings: *tn = TN (output columns per tile), *tiles_m_max = the bound on
+ * 256-row tiles over all routings (ceil(M/256) + E), *tiles_n = column tiles
+ * per expert. Host-only, no CUDA call; MXFP8_EINVAL for sizes the entry point
+ * rejects or null pointers.
+ */
+int mxfp8_grouped_gemm_tile_config(int E, int N, int K, int64_t M, int* tn, int* tiles_m_max, int* tiles_n);
+
+/*
  * Fused quantise-and-transpose from token-major bf16 (the layout in which the
  * forward and backward passes produce dY and X): x [M][R] bf16 (bit patterns,
  * 2-byte aligned) becomes q [R][M] E4M3 with the token axis contiguous

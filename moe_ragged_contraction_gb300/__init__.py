@@ -11,6 +11,7 @@ from ._lib import (  # noqa: F401
     Mxfp8Error,
     device_status,
     grouped_gemm,
+    grouped_gemm_tile_config,
     lib_path,
     load,
     quantize_tokenwise,

@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.mxfp8_wgrad_set_tile_rows.restype = I
         lib.mxfp8_wgrad_tile_config.argtypes = [I, I, I, L, IP, IP, IP, IP]
         lib.mxfp8_wgrad_tile_config.restype = I
+        lib.mxfp8_grouped_gemm_tile_config.argtypes = [I, I, I, L, IP, IP, IP]
+        lib.mxfp8_grouped_gemm_tile_config.restype = I
         _lib = lib
         return lib
 
@@ -196,6 +198,14 @@ def tile_config(E: int, N: int, K: int, M: int) -> dict:
     check(load().mxfp8_wgrad_tile_config(E, N, K, M, *(ctypes.byref(x) for x in v)))
     kn, tn, tm, tnn = (int(x.value) for x in v)
     return {"kn": kn, "tn": tn, "tiles_m": tm, "tiles_n": tnn}
+
+
+def grouped_gemm_tile_config(E: int, N: int, K: int, M: int) -> dict:
+    """Tiling the grouped GEMM would use for X [M, K] and W [E, N, K] under the current settings."""
+    v = [ctypes.c_int(0) for _ in range(3)]
+    check(load().mxfp8_grouped_gemm_tile_config(E, N, K, M, *(ctypes.byref(x) for x in v)))
+    tn, tm, tnn = (int(x.value) for x in v)
+    return {"tn": tn, "tiles_m_max": tm, "tiles_n": tnn}
 
 
 def quantize_tokenwise(x, q=None, s=None, stream=None):

@@ -372,6 +372,19 @@ int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8
     return MXFP8_OK;
 }
 
+int mxfp8_grouped_gemm_tile_config(int E, int N, int K, int64_t M, int* tn, int* tiles_m_max, int* tiles_n) {
+    if (!tn || !tiles_m_max || !tiles_n) return fail(MXFP8_EINVAL, "null pointer argument");
+    mxw::TileConfig tc;
+    mxw::GemmLayout lay;
+    if (E < 1 || E > MXFP8_MAX_EXPERTS || N < 1 || (N % 8) != 0 || K < 32 || (K % 32) != 0 || M < 1 ||
+        !mxw::choose_gemm_tiles(N, K, E, M, tile_rows_setting(), &tc) || !mxw::gemm_layout(E, N, K, M, tc, &lay))
+        return fail(MXFP8_EINVAL, "unsupported sizes E=%d N=%d K=%d M=%lld", E, N, K, (long long)M);
+    *tn = tc.tn;
+    *tiles_m_max = lay.mtiles_max;
+    *tiles_n = tc.tiles_n;
+    return MXFP8_OK;
+}
+
 int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, const uint8_t* sW,
                        const int32_t* offs, int E, int64_t M, int N, int K, uint16_t* out, void* stream) {
     if (E < 1 || E > MXFP8_MAX_EXPERTS) return fail(MXFP8_EINVAL, "E=%d out of range [1, %d]", E, MXFP8_MAX_EXPERTS);

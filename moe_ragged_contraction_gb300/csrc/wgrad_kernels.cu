@@ -1322,13 +1322,52 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
 
 // ------------------------------------------------------------- grouped GEMM host side
 
+// Measured cost of one tile of the grouped GEMM (row tiles of 256, a short
+// contraction of K/128 steps: 11-56 on the expert shapes), in microseconds
+// at about 1.9 GHz: a fixed hand-over part a(tn) and b(tn) per K-step, fitted
+// on GB300 over the forward and data-gradient products of the 16B and 671B
+// expert layers (tn = 128 .. 448 with 32-byte output stores where tn % 32 ==
+// 0). With one accumulator every tile waits for the previous tile's TMEM
+// drain, which short tiles do not amortise; widths of 16 mod 32 store in
+// 16-byte pieces, part of which falls inside that wait.
+double gemm_tile_cost(int tn, bool wide_ok, double steps) {
+    static const double ab[][2] = {
+        // tn = 128, 144, ..., 448
+        {1.02, 0.318}, {1.13, 0.322}, {1.00, 0.329}, {1.39, 0.338}, {0.93, 0.344}, {1.57, 0.359},
+        {1.57, 0.361}, {2.06, 0.382}, {1.19, 0.419}, {4.66, 0.487}, {3.16, 0.477}, {5.28, 0.476},
+        {2.86, 0.506}, {4.89, 0.498}, {3.23, 0.519}, {5.12, 0.532}, {3.12, 0.539}, {5.25, 0.553},
+        {2.46, 0.624}, {4.61, 0.638}, {2.87, 0.630}};
+    if (tn < 128) {
+        // narrower than measured: the long-tile column cost, scaled from tn = 128
+        const double b = ab[0][1] * (tn * column_cost(tn)) / (128.0 * column_cost(128));
+        return ab[0][0] + b * steps;
+    }
+    double a = ab[(tn - 128) / 16][0];
+    const double b = ab[(tn - 128) / 16][1];
+    // output rows not 16-column aligned: no 32-byte stores for any width
+    if (!wide_ok && tn % 32 == 0) a = tn > 256 ? (a > 5.0 ? a : 5.0) : a + 0.5;
+    return a + b * steps;
+}
+
 bool choose_gemm_tiles(int N, int K, int E, int64_t M, int force_tn, TileConfig* tc) {
     if (N < 1 || K < 32 || E < 1 || M < 1) return false;
-    const double ksteps = static_cast<double>((K + BK - 1) / BK);
-    double cost;
-    *tc = best_of(0, static_cast<int>(M < (int64_t(1) << 30) ? M : (int64_t(1) << 30)), N, ksteps, force_tn,
-                  N % 16 == 0, &cost);
-    return cost >= 0;
+    if (force_tn && (force_tn < 16 || force_tn > MAX_TN || force_tn % 16)) return false;
+    const double steps = static_cast<double>((K + BK - 1) / BK);
+    const int rows_m = static_cast<int>(M < (int64_t(1) << 30) ? M : (int64_t(1) << 30));
+    const bool wide_ok = N % 16 == 0;
+    double best = -1.0;
+    for (int tn = MAX_TN; tn >= 16; tn -= 16) {
+        if (force_tn && tn != force_tn) continue;
+        Geometry g;
+        if (!geometry(tn, &g)) continue;
+        // the row tiles are the same for every width: cost per row tile
+        const double c = static_cast<double>((N + tn - 1) / tn) * gemm_tile_cost(tn, wide_ok, steps);
+        if (best < 0 || c < best * (1.0 - 1e-9)) {
+            best = c;
+            *tc = make_config(0, tn, rows_m, N);
+        }
+    }
+    return best >= 0;
 }
 
 bool gemm_layout(int E, int N, int K, int64_t M, const TileConfig& tc, GemmLayout* L) {

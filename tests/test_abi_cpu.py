@@ -188,3 +188,52 @@ def test_quantize_transpose_validation(lib):
     assert q(None, 1024, 64, P, P, None) == _lib.EINVAL   # null x
     assert q(P + 1, 1024, 64, P, P, None) == _lib.EALIGN  # x not 2-byte aligned
     assert q(P, 1024, 64, P + 8, P, None) == _lib.EALIGN  # q not 16-byte aligned
+
+
+def test_grouped_gemm_validation(lib):
+    """Argument checks of the ragged-row grouped GEMM, all taken on the host
+    before any device call."""
+    f = lib.mxfp8_grouped_gemm
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_void_p, ctypes.c_void_p]
+    ok = (P, P, P, P, P)
+    assert f(*ok, 0, 1024, 256, 512, P, None) == _lib.EINVAL      # E < 1
+    assert f(*ok, 2049, 1024, 256, 512, P, None) == _lib.EINVAL   # E above the maximum
+    assert f(*ok, 4, 0, 256, 512, P, None) == _lib.EINVAL         # M < 1
+    assert f(*ok, 4, 1 << 31, 256, 512, P, None) == _lib.EINVAL   # M above int32
+    assert f(*ok, 4, 1024, 256, 500, P, None) == _lib.EINVAL      # K % 32 != 0
+    assert f(*ok, 4, 1024, 0, 512, P, None) == _lib.EINVAL        # N < 1
+    assert f(P, P, None, P, P, 4, 1024, 256, 512, P, None) == _lib.EINVAL  # null W
+    assert f(P, P, P, P, P, 4, 1024, 256, 512, None, None) == _lib.EINVAL  # null out
+    assert f(P + 8, P, P, P, P, 4, 1024, 256, 512, P, None) == _lib.EALIGN  # X not 16-byte aligned
+    assert f(*ok, 4, 1024, 260, 512, P, None) == _lib.EALIGN      # N % 8 != 0 (output rows)
+    assert f(*ok, 4, 1024, 256, 512, P + 2, None) == _lib.EALIGN  # out not 16-byte aligned
+
+
+def test_grouped_gemm_tile_choice(lib):
+    """Host-side tiling of the ragged-row grouped GEMM: the measured
+    short-contraction cost (a per-tile hand-over plus a per-K-step part)
+    decides the width; the row-tile bound is ceil(M/256) + E; a forced width
+    is honoured; sizes the entry point rejects fail."""
+    try:
+        mx.set_tile_rows(0)
+        # 16B forward (hidden 2048 -> 1408): 4 tiles of 352, 32-byte stores
+        assert mx.grouped_gemm_tile_config(8, 1408, 2048, 32768) == {"tn": 352, "tiles_m_max": 136, "tiles_n": 4}
+        # 16B data gradient (1408 -> 2048, 11 K-steps): one 256-wide MMA per chunk
+        assert mx.grouped_gemm_tile_config(8, 2048, 1408, 32768) == {"tn": 256, "tiles_m_max": 136, "tiles_n": 8}
+        # 671B up/gate forward (7168 -> 4096) and data gradient (4096 -> 7168)
+        assert mx.grouped_gemm_tile_config(32, 4096, 7168, 262144)["tn"] == 384
+        assert mx.grouped_gemm_tile_config(32, 7168, 4096, 262144)["tn"] == 448
+        # 671B down forward (2048 -> 7168) and data gradient (7168 -> 2048)
+        assert mx.grouped_gemm_tile_config(32, 7168, 2048, 524288) == {"tn": 448, "tiles_m_max": 2080, "tiles_n": 16}
+        assert mx.grouped_gemm_tile_config(32, 2048, 7168, 524288)["tn"] == 416
+        # narrow outputs: one column tile
+        assert mx.grouped_gemm_tile_config(16, 64, 128, 900) == {"tn": 64, "tiles_m_max": 20, "tiles_n": 1}
+        mx.set_tile_rows(224)
+        assert mx.grouped_gemm_tile_config(8, 1408, 2048, 32768) == {"tn": 224, "tiles_m_max": 136, "tiles_n": 7}
+        mx.set_tile_rows(0)
+        for bad in ((0, 256, 512, 1024), (4, 260, 512, 1024), (4, 256, 500, 1024), (4, 256, 512, 0)):
+            with pytest.raises(mx.Mxfp8Error):
+                mx.grouped_gemm_tile_config(*bad)
+    finally:
+        mx.set_tile_rows(0)
