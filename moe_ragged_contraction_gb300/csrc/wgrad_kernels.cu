@@ -52,6 +52,26 @@ constexpr int PREP_THREADS = 256;
 constexpr int PREP_ROWS = 128;        // rows of one scale-factor block
 constexpr int PREP_TILE_STEPS = 32;   // K-steps per gather task (one per lane)
 
+// The block's contiguous share of the 16-byte-aligned interior of
+// [p, p + bytes), streamed into L2 in 4 KB bulk prefetches (one per thread at
+// a time). The gathers below read 128-byte pieces of rows that lie far apart;
+// straight from DRAM such pieces each open a page and run at a fraction of
+// the streaming rate, after this they hit L2. The few edge bytes outside the
+// aligned interior are simply not prefetched (nothing outside the buffer is
+// touched).
+__device__ __forceinline__ void prefetch_share_l2(const uint8_t* p, size_t bytes) {
+    constexpr size_t PIECE = 4096;
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15);
+    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
+    if (bytes < 16 || a1 <= a0) return;
+    const size_t n = a1 - a0;
+    const size_t share = ((n + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+    const size_t lo = share * blockIdx.x;
+    const size_t hi = lo + share < n ? lo + share : n;
+    for (size_t o = lo + threadIdx.x * PIECE; o < hi; o += PREP_THREADS * PIECE)
+        bulk_prefetch_l2(reinterpret_cast<const void*>(a0 + o), static_cast<uint32_t>(hi - o < PIECE ? hi - o : PIECE));
+}
+
 struct PrepSide {
     const uint8_t* plane;  // scale plane [rows][M/32]
     uint8_t* sf;           // scale-factor blocks [tiles][ts_max][blocks][512 B]
@@ -60,24 +80,21 @@ struct PrepSide {
 };
 
 // Four scale bytes starting at byte `off` of the plane (which holds `size`
-// bytes): one aligned 32-bit load, or two and a funnel shift when the bytes
-// straddle a word (alignment is taken on the absolute address, so an
-// unaligned plane is fine: rounding down never leaves its allocation); byte
-// loads where a word would run past the end of the plane.
-__device__ __forceinline__ uint32_t load_scale4(const uint8_t* __restrict__ plane, size_t off, size_t size) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(plane) + off;
-    const uintptr_t w = a & ~uintptr_t(3);
-    const uint32_t sh = static_cast<uint32_t>(a & 3) * 8;
-    const uintptr_t end = reinterpret_cast<uintptr_t>(plane) + size;
-    if (w + (sh ? 8 : 4) <= end) {
-        const uint32_t lo = __ldg(reinterpret_cast<const uint32_t*>(w));
-        if (sh == 0) return lo;
-        const uint32_t hi = __ldg(reinterpret_cast<const uint32_t*>(w + 4));
-        return __funnelshift_r(lo, hi, sh);
-    }
+// bytes), for rows at the end of a plane where an aligned word could run past
+// it: four predicated byte loads (bytes at or past the end, or all four when
+// `ok` is false, read as 0), no branch, so that a thread's loads for all its
+// rows stay in flight together. Everywhere else the gathers read two aligned
+// words and funnel-shift them (alignment taken on the absolute address, so an
+// unaligned plane is fine: rounding down never leaves its allocation).
+__device__ __forceinline__ uint32_t load_scale4_edge(const uint8_t* __restrict__ plane, size_t off, size_t size,
+                                                     bool ok) {
     uint32_t v = 0;
-    for (int kb = 0; kb < 4; ++kb)
-        if (off + kb < size) v |= static_cast<uint32_t>(__ldg(plane + off + kb)) << (8 * kb);
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+        const bool in = ok && off + kb < size;
+        const uint32_t b = in ? static_cast<uint32_t>(__ldg(plane + (in ? off + kb : 0))) : 0u;
+        v |= b << (8 * kb);
+    }
     return v;
 }
 
@@ -102,6 +119,14 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     const unsigned full = 0xffffffffu;
     const int Mi = static_cast<int>(M);
 
+    prefetch_share_l2(sm_side.plane, static_cast<size_t>(sm_side.rows) * static_cast<size_t>(M / 32));
+    prefetch_share_l2(sn_side.plane, static_cast<size_t>(sn_side.rows) * static_cast<size_t>(M / 32));
+    // the main kernel may launch now: its prologue (barriers, TMEM, tensor
+    // maps) overlaps this kernel, and it waits for this grid's completion (and
+    // the visibility of its writes) before it reads the plan or the scales.
+    // Every block of this grid is resident once all have passed here, so the
+    // main kernel's CTAs only queue behind them for shared memory.
+    griddep_launch_dependents();
     for (int g = threadIdx.x; g < E; g += PREP_THREADS) s_end[g] = offs[g];
     __syncthreads();
     if (warp == 0) {
@@ -218,13 +243,35 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         const uint32_t keep = nvalid >= 4 ? 0xffffffffu : ((1u << (8 * nvalid)) - 1u);
         const size_t plane_bytes = static_cast<size_t>(rows) * static_cast<size_t>(sM);
         constexpr int ROWS_PER_WARP = PREP_ROWS / (PREP_THREADS / 32);
+        // rows of the plane this block may read: inside its tile and the plane
+        const int rows_lim = min(rows, row0 - in_tile0 + tile_rows);
         uint32_t wv[ROWS_PER_WARP];
+        if (nvalid > 0 && static_cast<size_t>(rows_lim - 1) * sM + col + 8 <= plane_bytes) {
+            // every word this lane reads lies inside the plane: rows past the
+            // limit read the last valid row and are zeroed afterwards
+            // all loads first, then the shifts: the words of every row in flight together
+            uint32_t lo[ROWS_PER_WARP], hi[ROWS_PER_WARP], sh[ROWS_PER_WARP];
 #pragma unroll
-        for (int i = 0; i < ROWS_PER_WARP; ++i) {
-            const int r = warp + i * (PREP_THREADS / 32);
-            const int row = row0 + r;
-            const bool ok = nvalid > 0 && in_tile0 + r < tile_rows && row < rows;
-            wv[i] = ok ? (load_scale4(plane, static_cast<size_t>(row) * sM + col, plane_bytes) & keep) : 0u;
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int row = min(row0 + warp + i * (PREP_THREADS / 32), rows_lim - 1);
+                const uintptr_t a = reinterpret_cast<uintptr_t>(plane) + static_cast<size_t>(row) * sM + col;
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+                lo[i] = __ldg(w);
+                hi[i] = __ldg(w + 1);
+                sh[i] = static_cast<uint32_t>(a & 3) * 8;
+            }
+#pragma unroll
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int row = row0 + warp + i * (PREP_THREADS / 32);
+                wv[i] = row < rows_lim ? (__funnelshift_r(lo[i], hi[i], sh[i]) & keep) : 0u;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int row = row0 + warp + i * (PREP_THREADS / 32);
+                const bool ok = nvalid > 0 && row < rows_lim;
+                wv[i] = load_scale4_edge(plane, ok ? static_cast<size_t>(row) * sM + col : 0, plane_bytes, ok) & keep;
+            }
         }
 #pragma unroll
         for (int i = 0; i < ROWS_PER_WARP; ++i)
@@ -243,11 +290,6 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         }
         __syncthreads();
     }
-    // This block's work is done: once every block got here the main kernel
-    // may launch and run its prologue (it waits for this grid's completion
-    // before reading anything written here). Triggering earlier would let its
-    // resident CTAs crowd this kernel off the SMs.
-    griddep_launch_dependents();
 }
 
 // ============================================================== grouped GEMM prep
@@ -283,6 +325,9 @@ __global__ void __launch_bounds__(PREP_THREADS) gemm_prep(const GemmPrepArgs a) 
     const int E = a.E;
     const long long M = a.M;
 
+    prefetch_share_l2(a.sX, static_cast<size_t>(M) * static_cast<size_t>(a.K / 32));
+    prefetch_share_l2(a.sW, static_cast<size_t>(E) * a.N * static_cast<size_t>(a.K / 32));
+    griddep_launch_dependents();  // as in wgrad_prep: the main kernel's prologue overlaps this grid
     for (int g = threadIdx.x; g < E; g += PREP_THREADS) s_end[g] = a.offs[g];
     __syncthreads();
     if (warp == 0) {
@@ -399,11 +444,31 @@ __global__ void __launch_bounds__(PREP_THREADS) gemm_prep(const GemmPrepArgs a) 
         const uint32_t keep = nvalid >= 4 ? 0xffffffffu : ((1u << (8 * nvalid)) - 1u);
         constexpr int ROWS_PER_WARP = PREP_ROWS / (PREP_THREADS / 32);
         uint32_t wv[ROWS_PER_WARP];
+        if (nvalid > 0 && rows_valid > 0 &&
+            static_cast<size_t>(row0 + rows_valid - 1) * sK + 4 * s + 8 <= plane_bytes) {
+            // all of this lane's words inside the plane (see wgrad_prep)
+            uint32_t lo[ROWS_PER_WARP], hi[ROWS_PER_WARP], sh[ROWS_PER_WARP];
 #pragma unroll
-        for (int i = 0; i < ROWS_PER_WARP; ++i) {
-            const int r = warp + i * (PREP_THREADS / 32);
-            const bool ok = nvalid > 0 && r < rows_valid;
-            wv[i] = ok ? (load_scale4(plane, static_cast<size_t>(row0 + r) * sK + 4 * s, plane_bytes) & keep) : 0u;
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int r = min(warp + i * (PREP_THREADS / 32), rows_valid - 1);
+                const uintptr_t ad = reinterpret_cast<uintptr_t>(plane) + static_cast<size_t>(row0 + r) * sK + 4 * s;
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(ad & ~uintptr_t(3));
+                lo[i] = __ldg(w);
+                hi[i] = __ldg(w + 1);
+                sh[i] = static_cast<uint32_t>(ad & 3) * 8;
+            }
+#pragma unroll
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int r = warp + i * (PREP_THREADS / 32);
+                wv[i] = r < rows_valid ? (__funnelshift_r(lo[i], hi[i], sh[i]) & keep) : 0u;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int r = warp + i * (PREP_THREADS / 32);
+                const bool ok = nvalid > 0 && r < rows_valid;
+                wv[i] = load_scale4_edge(plane, ok ? static_cast<size_t>(row0 + r) * sK + 4 * s : 0, plane_bytes, ok) & keep;
+            }
         }
 #pragma unroll
         for (int i = 0; i < ROWS_PER_WARP; ++i)
@@ -429,7 +494,6 @@ __global__ void __launch_bounds__(PREP_THREADS) gemm_prep(const GemmPrepArgs a) 
              i += static_cast<long long>(gridDim.x) * PREP_THREADS)
             z[i] = make_uint4(0, 0, 0, 0);
     }
-    griddep_launch_dependents();
 }
 
 // ============================================================== main kernel
