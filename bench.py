@@ -626,7 +626,7 @@ def bench_gemm(args):
             "pct_of_mxfp8_peak": 100.0 * value / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": peak_src, "kernel": "wgrad_main (row-tile mode)",
-                         "algorithmic_flop_per_launch": flop_call, "traffic": None,
+                         "algorithmic_flop_per_launch": flop_call, "traffic": measured_traffic("gemm:" + args.config),
                          "forward_main_ms": fwd_ms, "dgrad_main_ms": dgr_ms,
                          "forward_tflops": flop_call / (fwd_ms * 1e-3) / 1e12,
                          "dgrad_tflops": flop_call / (dgr_ms * 1e-3) / 1e12},
