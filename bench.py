@@ -2,8 +2,8 @@
 
 One step = one full call of the hot path (plan + scale re-layout kernel and
 the main tcgen05 contraction kernel) over one batch of synthetic input that is
-already resident in HBM; the L2 is flushed (a 256 MiB write) before every
-timed step, outside the timed interval. Quantisation builds the inputs and is
+already resident in HBM; the L2 is flushed (a 256 MiB write, then a 256 MiB
+read) before every timed step, outside the timed interval. Quantisation builds the inputs and is
 not timed ("Ragged MXFP8 Weight Gradients", section 7: operator time on
 pre-quantised operands).
 
@@ -36,6 +36,27 @@ METRIC = "TFLOP/s (2*N*K*sum(M_g)) ragged MXFP8 wgrad, % of GB300 MXFP8 tensor p
 FP8_OVER_BF16 = 2.0  # nominal dense ratio: 4.5 PF fp8 / 2.25 PF bf16
 L2_FLUSH_BYTES = 256 << 20
 MAIN_KERNEL_SRC = os.path.join(ROOT, "moe_ragged_contraction_gb300", "csrc", "wgrad_kernels.cu")
+
+
+class L2Flush:
+    """Evicts the L2 between timed steps (outside the timed interval): a
+    256 MiB write (larger than the 129 MB L2), then a 256 MiB read of another
+    buffer, which leaves the L2 holding only clean lines of that buffer. The
+    timed step then starts with none of its inputs in L2 and without the
+    write's dirty lines still draining to HBM underneath it (measured: they
+    cost the 16B step about 3 us)."""
+
+    DESCRIPTION = "flushed before every timed step (256 MiB write, then 256 MiB read)"
+
+    def __init__(self, device):
+        import torch
+
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 def kernel_source_hash() -> str:
@@ -235,7 +256,7 @@ def bench_gpu(args):
     w = I.WORKLOADS[args.config]
     A, sA, B, sB, offs = make_device_inputs(args.config, device)
     out = torch.empty((w.E, w.N, w.K), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream(device)
 
     def step(main_pair=None):
@@ -252,7 +273,7 @@ def bench_gpu(args):
     time.sleep(0.3)
     # warm-up: W steps, then ~0.5 s of back-to-back calls so clocks settle
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     t_end = time.perf_counter() + 0.5
@@ -277,7 +298,7 @@ def bench_gpu(args):
     # per-call enqueue latency (the end-to-end figure below includes that).
     hold_gpu(K)
     for i in range(K):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -291,7 +312,7 @@ def bench_gpu(args):
     # kernel, so this is its full launch-to-end time)
     hold_gpu(K)
     for i in range(K):
-        flush.zero_()
+        flush()
         step(main_pair=evm[i])
     torch.cuda.synchronize()
     main_ms = [a.elapsed_time(b) for a, b in evm]
@@ -369,7 +390,7 @@ def bench_gpu(args):
             "dtype": "mxfp8_e4m3 (e8m0 block-32 scales), fp32 accumulate, bf16 out",
             "data": "synthetic (seeded routing and N(0,1)/Student-t operands, quantised on the GPU)",
             "config": {"workload": args.config, "E": w.E, "N": w.N, "K": w.K, "M": w.M,
-                       "routing": w.description, "l2": "flushed (256 MiB write) before every timed step",
+                       "routing": w.description, "l2": L2Flush.DESCRIPTION,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_mxfp8_peak": 100.0 * value / world / peak,
             "roofline": roof,
@@ -402,7 +423,7 @@ def bench_comparators(args):
     mx.build()
     mx.load()
     w = I.WORKLOADS[args.config]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
 
     def timed(fn, steps):
         for _ in range(3):
@@ -410,7 +431,7 @@ def bench_comparators(args):
         torch.cuda.synchronize()
         tot = 0.0
         for _ in range(steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -487,21 +508,21 @@ def bench_quantizer(args):
     sa = torch.empty((w.N, w.M // 32), dtype=torch.uint8, device=device)
     qb = torch.empty((w.K, w.M), dtype=torch.uint8, device=device)
     sb = torch.empty((w.K, w.M // 32), dtype=torch.uint8, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
 
     def step():
         mx.quantize_transpose_bf16(dy, qa, sa)
         mx.quantize_transpose_bf16(x, qb, sb)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     hold_gpu(K)
     for i in range(K):
-        flush.zero_()
+        flush()
         ev[i][0].record()
         step()
         ev[i][1].record()
@@ -515,7 +536,7 @@ def bench_quantizer(args):
     return {"metric": "GB/s fused bf16 quantise-and-transpose (operands of the wgrad)", "value": gbs,
             "unit": "GB/s", "ms_per_step": ms, "steps": K, "warmup": args.warmup,
             "config": {"workload": args.config, "M": w.M, "N": w.N, "K": w.K,
-                       "l2": "flushed (256 MiB write) before every timed step"},
+                       "l2": L2Flush.DESCRIPTION},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "algorithmic_bytes_per_step": alg, "kernel": "quantize_transpose_bf16_kernel"},
             "gpu_launches": 2 * K}
@@ -565,7 +586,7 @@ def bench_gemm(args):
     offs = torch.from_numpy(I.offsets(I.group_sizes(args.config))).to(device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream(device)
 
     def step(pairs=None):
@@ -580,7 +601,7 @@ def bench_gemm(args):
     sampler.start()
     time.sleep(0.3)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     S = args.steps
@@ -594,7 +615,7 @@ def bench_gemm(args):
     torch.cuda.synchronize()
     hold_gpu(2 * S)
     for i in range(S):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -602,7 +623,7 @@ def bench_gemm(args):
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     hold_gpu(2 * S)
     for i in range(S):
-        flush.zero_()
+        flush()
         step(pairs=evm[i])
     torch.cuda.synchronize()
     fwd_ms = float(np.mean([p[0][0].elapsed_time(p[0][1]) for p in evm]))
@@ -622,7 +643,7 @@ def bench_gemm(args):
             "config": {"workload": args.config, "E": E, "N": N, "K": K, "M": M, "routing": w.description,
                        "forward": f"[{M},{K}] x [{E},{N},{K}]^T -> [{M},{N}]",
                        "dgrad": f"[{M},{N}] x [{E},{K},{N}]^T -> [{M},{K}]",
-                       "l2": "flushed (256 MiB write) before every timed step"},
+                       "l2": L2Flush.DESCRIPTION},
             "pct_of_mxfp8_peak": 100.0 * value / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": peak_src, "kernel": "wgrad_main (row-tile mode)",
