@@ -254,6 +254,20 @@ int mxfp8_wgrad_set_tile_orientation(int mode);
 int mxfp8_wgrad_set_tile_rows(int tn);
 int mxfp8_wgrad_tile_config(int E, int N, int K, int64_t M, int* kn, int* tn, int* tiles_m, int* tiles_n);
 
+/*
+ * Epilogue stores (process-wide, every later call of mxfp8_wgrad_grouped{,_ws,
+ * _noalloc} and mxfp8_grouped_gemm): mode 0 (default) narrows each 32 x 32
+ * block of the accumulator into a shared-memory staging buffer and writes it
+ * with a TMA store, wherever the staging fits beside the operand pipeline
+ * without costing a stage (the 256-row side on A, out 16-byte aligned, output
+ * rows a multiple of 8 elements); blocks that straddle a tile, group or output
+ * edge, and all other tilings, store straight from registers. Mode 1 stores
+ * straight from registers always. The results are the same bits either way.
+ * The initial mode comes from MXFP8_EPILOGUE_STORE ("auto" or "direct").
+ * MXFP8_EINVAL for other modes.
+ */
+int mxfp8_wgrad_set_epilogue_store(int mode);
+
 /* Measurement hook: when both events are non-NULL, the next
  * mxfp8_wgrad_grouped{,_ws} call on this thread records `ev_before` on its
  * stream right before the main contraction kernel and `ev_after` right after

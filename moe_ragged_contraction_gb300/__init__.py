@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     load,
     quantize_tokenwise,
     quantize_transpose_bf16,
+    set_epilogue_store,
     set_tile_orientation,
     set_tile_rows,
     set_timing_events,

@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
         IP = ctypes.POINTER(ctypes.c_int)
         lib.mxfp8_wgrad_set_tile_rows.argtypes = [I]
         lib.mxfp8_wgrad_set_tile_rows.restype = I
+        lib.mxfp8_wgrad_set_epilogue_store.argtypes = [I]
+        lib.mxfp8_wgrad_set_epilogue_store.restype = I
         lib.mxfp8_wgrad_tile_config.argtypes = [I, I, I, L, IP, IP, IP, IP]
         lib.mxfp8_wgrad_tile_config.restype = I
         lib.mxfp8_grouped_gemm_tile_config.argtypes = [I, I, I, L, IP, IP, IP]
@@ -190,6 +192,14 @@ def set_tile_orientation(mode: int) -> None:
 def set_tile_rows(tn: int) -> None:
     """Process-wide N-side tile width: 0 for the modelled choice, else a multiple of 16 in [16, 448]."""
     check(load().mxfp8_wgrad_set_tile_rows(int(tn)))
+
+
+STORE_AUTO, STORE_DIRECT = 0, 1
+
+
+def set_epilogue_store(mode: int) -> None:
+    """Process-wide epilogue stores: 0 TMA stores where their staging fits, 1 direct stores only."""
+    check(load().mxfp8_wgrad_set_epilogue_store(int(mode)))
 
 
 def tile_config(E: int, N: int, K: int, M: int) -> dict:

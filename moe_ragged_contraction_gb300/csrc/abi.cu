@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <atomic>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -113,6 +114,23 @@ int make_operand_map3(CUtensorMap* map, const uint8_t* base, int64_t row_len, in
     return MXFP8_OK;
 }
 
+// bf16 output viewed as [depth][rows][cols] for the TMA-store epilogue: boxes
+// of 32 columns x 32 rows x 1, 64-byte swizzle (the staging layout the
+// epilogue writes). Returns 0 when the layout does not allow a tensor map
+// (rows of cols bf16 not a multiple of 16 bytes, or out not 16-byte aligned).
+int make_out_map(CUtensorMap* map, uint16_t* out, int64_t cols, int64_t rows, int64_t depth) {
+    if ((cols % 8) != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0) return 0;
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    if (get_encoder(&enc)) return 0;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(depth)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(cols) * rows * 2};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 1 : 0;
+}
+
 // Scale-factor workspace viewed as u32 [blocks][128] (one 512-byte block per
 // row); boxes of box_blocks whole blocks, no swizzle.
 int make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t blocks, int box_blocks) {
@@ -175,6 +193,22 @@ std::atomic<int> g_orientation{-1};
 // N-side tile rows forced by mxfp8_wgrad_set_tile_rows (0 = modelled best);
 // the initial value comes from MXFP8_TILE_ROWS (ignored unless admissible).
 std::atomic<int> g_tile_rows{-1};
+// Epilogue stores (mxfp8_wgrad_set_epilogue_store): 0 = TMA stores where their
+// staging fits, 1 = direct stores only; the initial value comes from
+// MXFP8_EPILOGUE_STORE ("auto" or "direct"; default auto).
+std::atomic<int> g_store_mode{-1};
+
+int store_mode() {
+    int m = g_store_mode.load(std::memory_order_relaxed);
+    if (m < 0) {
+        const char* s = getenv("MXFP8_EPILOGUE_STORE");
+        int v = (s && strcmp(s, "direct") == 0) ? 1 : 0;
+        int expected = -1;
+        g_store_mode.compare_exchange_strong(expected, v);
+        m = g_store_mode.load(std::memory_order_relaxed);
+    }
+    return m;
+}
 
 int orientation_mode() {
     int m = g_orientation.load(std::memory_order_relaxed);
@@ -277,7 +311,7 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     }
     // M side: 256-row pair tiles, 128 rows per CTA; N side: tn-row tiles, per CTA
     // n1/2 rows for the first MMA and n2/2 for the second
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     const uint8_t* m_op = tc.kn ? B : A;
     const uint8_t* n_op = tc.kn ? A : B;
     const int n_rows = tc.kn ? N : K;
@@ -305,6 +339,9 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     a.ev_before = evb;
     a.ev_after = eva;
     a.stall_first_stage = stall;
+    // output as [E][N][K] for the TMA-store epilogue (used where its staging fits)
+    a.tma_store = (store_mode() == 0 && make_out_map(&maps[5], out, K, N, E)) ? 1 : 0;
+    if (!a.tma_store) maps[5] = maps[0];
     const char* what = "";
     cudaError_t e = mxw::launch_wgrad(a, maps, &what);
     if (e != cudaSuccess) return fail_cuda(e, what);
@@ -329,6 +366,12 @@ size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M) {
 int mxfp8_wgrad_set_tile_orientation(int mode) {
     if (mode < 0 || mode > 2) return fail(MXFP8_EINVAL, "tile orientation mode %d not in {0, 1, 2}", mode);
     g_orientation.store(mode, std::memory_order_relaxed);
+    return MXFP8_OK;
+}
+
+int mxfp8_wgrad_set_epilogue_store(int mode) {
+    if (mode < 0 || mode > 1) return fail(MXFP8_EINVAL, "epilogue store mode %d not in {0, 1}", mode);
+    g_store_mode.store(mode, std::memory_order_relaxed);
     return MXFP8_OK;
 }
 
@@ -411,7 +454,7 @@ int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, co
     if (rc) return rc;
     // X: 256-row tiles, 128 rows per CTA; W as [E][N][K]: per CTA n1/2 rows for the
     // first MMA and n2/2 for the second
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     rc = make_operand_map(&maps[0], X, static_cast<int>(M), K, mxw::BM);
     if (rc) return rc;
     rc = make_operand_map3(&maps[1], W, K, N, E, tc.n1 / 2);
@@ -435,6 +478,9 @@ int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, co
     a.stream = st;
     a.ev_before = evb;
     a.ev_after = eva;
+    // output as [1][M][N] for the TMA-store epilogue (used where its staging fits)
+    a.tma_store = (store_mode() == 0 && make_out_map(&maps[5], out, N, M, 1)) ? 1 : 0;
+    if (!a.tma_store) maps[5] = maps[0];
     const char* what = "";
     cudaError_t e = mxw::launch_gemm(a, maps, &what);
     if (e != cudaSuccess) return fail_cuda(e, what);

@@ -68,6 +68,7 @@ struct WgradArgs {
     cudaStream_t stream;
     cudaEvent_t ev_before, ev_after;
     int stall_first_stage;  // failure-path test hook (0 in normal use)
+    int tma_store;          // maps[5] describes out: TMA-store epilogue where its staging fits
 };
 
 // Enqueue the plan / scale re-layout kernel and the main contraction kernel.
@@ -104,6 +105,7 @@ struct GemmArgs {
     uint64_t wait_limit_ns;
     cudaStream_t stream;
     cudaEvent_t ev_before, ev_after;
+    int tma_store;          // as in WgradArgs
 };
 
 // maps: X (boxes of BM rows x BK), W as 3-D [E][N][K] (boxes of n1/2 and n2/2

@@ -519,6 +519,7 @@ constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 3;                        // producer, MMA issuer, stage watcher, then the epilogue
 constexpr int MAIN_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int MAX_STAGES = 7;
+constexpr uint32_t STG_CHUNK = 32 * 64;  // one epilogue chunk: 32 rows x 32 bf16 columns (64-byte swizzle)
 constexpr int MAIN_SMEM_MAX = 232448;  // the sm_100-family opt-in limit per CTA
 // Named barriers between the stage watcher and the MMA warp (64 threads each):
 // BAR_READY + st: stage st holds data (watcher arrives, MMA warp syncs);
@@ -554,8 +555,10 @@ struct MainParams {
     int stages, sf_slots;
     int acc_bufs;            // accumulators in TMEM (2: the next tile's MMAs overlap this tile's drain)
     int wide_stores;         // 32-byte output stores (rows of 16 columns 32-byte aligned), else 16-byte
+    int tma_store;           // epilogue chunks through shared memory and TMA stores (rows of A on the 256 side)
+    int stg_bufs;            // staging buffers per epilogue warp (1 or 2) when tma_store
     uint32_t sf_col0;        // first TMEM column of the scale-factor slots
-    uint32_t off_b, off_sfa, off_sfb, off_bar, b_stage;  // shared-memory layout (bytes)
+    uint32_t off_b, off_sfa, off_sfb, off_stg, off_bar, b_stage;  // shared-memory layout (bytes)
     unsigned long long wait_ns;
     int stall_first_stage;   // test hook: over-declare the first stage's bytes so its wait runs out
 };
@@ -791,12 +794,14 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
 
 // maps: M-side operand (boxes of 128 rows x BK tokens), N-side operand for the
 // first MMA (n1/2 rows) and for the second (n2/2 rows; unused when n2 == 0),
-// and the two sides' scale-factor blocks as u32 [blocks][128] (boxes of 1 and
-// nblk_n blocks).
+// the two sides' scale-factor blocks as u32 [blocks][128] (boxes of 1 and
+// nblk_n blocks), and the bf16 output as [depth][rows][columns] (boxes of 32 x
+// 32 x 1, 64-byte swizzle; used only when p.tma_store).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
     wgrad_main(const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmN1,
                const __grid_constant__ CUtensorMap tmN2, const __grid_constant__ CUtensorMap tmSFM,
-               const __grid_constant__ CUtensorMap tmSFN, const MainParams p) {
+               const __grid_constant__ CUtensorMap tmSFN, const __grid_constant__ CUtensorMap tmOut,
+               const MainParams p) {
     extern __shared__ uint8_t main_smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(main_smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -831,6 +836,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         if (p.n2) tma_prefetch_desc(&tmN2);
         tma_prefetch_desc(&tmSFM);
         tma_prefetch_desc(&tmSFN);
+        if (p.tma_store) tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -964,9 +970,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         auto epilogue_loop = [&](auto nbuf_tag, auto mode_tag) {
             constexpr uint32_t BUF_SHIFT = decltype(nbuf_tag)::value == 2 ? 1u : 0u;
             // 0: rows of A on the 256 side, 16-byte stores; 1: the same with
-            // 32-byte stores; 2: rows of B on the 256 side (transposed stores)
+            // 32-byte stores; 2: rows of B on the 256 side (transposed stores);
+            // 3: rows of A on the 256 side through shared memory and TMA stores
             constexpr int MODE = decltype(mode_tag)::value;
             uint32_t ntile = 0;  // non-empty tiles drained so far
+            // MODE 3: this warp's staging buffers (2 KB each) and the next one to fill
+            const uint32_t stg_warp =
+                sbase + p.off_stg + static_cast<uint32_t>((warp - EPI_WARP0) * p.stg_bufs) * STG_CHUNK;
+            uint32_t sbuf = 0;
             const bool odd = lane & 1;
             // (no look-ahead here: the item's loads overlap the wait for its
             // accumulator; 32-bit counters: the item count is below 2^31)
@@ -989,6 +1000,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                 // lane stores (k, k+1) of row n and the odd lane (k, k+1) of row
                 // n+1: 4-byte stores, 64 contiguous bytes per row and instruction.
                 auto store_chunk = [&](int j, const uint32_t (&v)[32]) {
+                    if (MODE == 3) {
+                        // whole 32 x 32 chunks (inside this warp's columns and, for
+                        // ragged rows, inside the group) go through a staging buffer:
+                        // lane = row, 64 bytes per row, 16-byte pieces placed by the
+                        // 64-byte swizzle (piece ^ bits 7-8 of the address), which
+                        // keeps the shared stores conflict-free; the TMA store
+                        // clips rows and columns outside the output
+                        const int row0w = it.m0 + static_cast<int>(rank) * BM + q * 32;
+                        // (a chunk that starts outside the output has nothing to store: the
+                        // checks of the 16-byte path below skip all of it)
+                        if (32 * j + 32 <= ncols && row0w < it.m_end && ncol0 + 32 * j < p.col_limit &&
+                            (p.mode == 0 || row0w + 32 <= it.m_end)) {
+                            if (lane == 0) {
+                                if (p.stg_bufs == 2) bulk_wait_group_read<1>();
+                                else bulk_wait_group_read<0>();
+                            }
+                            __syncwarp();
+                            const uint32_t buf = stg_warp + sbuf * STG_CHUNK;
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                const uint32_t piece = static_cast<uint32_t>(c4) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+                                st_shared_v4(buf + static_cast<uint32_t>(lane) * 64u + piece * 16u,
+                                             pack_bf16x2(v[8 * c4 + 0], v[8 * c4 + 1]),
+                                             pack_bf16x2(v[8 * c4 + 2], v[8 * c4 + 3]),
+                                             pack_bf16x2(v[8 * c4 + 4], v[8 * c4 + 5]),
+                                             pack_bf16x2(v[8 * c4 + 6], v[8 * c4 + 7]));
+                            }
+                            fence_proxy_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&tmOut, buf, ncol0 + 32 * j, row0w, p.mode == 0 ? it.g : 0);
+                                bulk_commit_group();
+                            }
+                            sbuf ^= static_cast<uint32_t>(p.stg_bufs - 1);
+                            return;
+                        }
+                        // partial chunks: the 16-byte stores below
+                    }
                     if (MODE == 1) {
                         // one full 32-byte sector per lane and store
 #pragma unroll
@@ -1001,7 +1050,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                                              pack_bf16x2(v[c + 10], v[c + 11]), pack_bf16x2(v[c + 12], v[c + 13]),
                                              pack_bf16x2(v[c + 14], v[c + 15]));
                         }
-                    } else if (MODE == 0) {
+                    } else if (MODE == 0 || MODE == 3) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             const int cc = 32 * j + c;
@@ -1067,17 +1116,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                 }
                 ++ntile;
             }
+            if (MODE == 3) {
+                // every TMA store of this warp has completed before the CTA may exit
+                if (lane == 0) bulk_wait_group_all();
+                __syncwarp();
+            }
         };
         using I1 = std::integral_constant<int, 1>;
         using I2 = std::integral_constant<int, 2>;
         using I0 = std::integral_constant<int, 0>;
-        switch ((p.acc_bufs == 2 ? 3 : 0) + (p.kn ? 2 : (p.wide_stores ? 1 : 0))) {
+        using I3 = std::integral_constant<int, 3>;
+        switch ((p.acc_bufs == 2 ? 4 : 0) + (p.kn ? 2 : (p.tma_store ? 3 : (p.wide_stores ? 1 : 0)))) {
             case 0: epilogue_loop(I1{}, I0{}); break;
             case 1: epilogue_loop(I1{}, I1{}); break;
             case 2: epilogue_loop(I1{}, I2{}); break;
-            case 3: epilogue_loop(I2{}, I0{}); break;
-            case 4: epilogue_loop(I2{}, I1{}); break;
-            default: epilogue_loop(I2{}, I2{}); break;
+            case 3: epilogue_loop(I1{}, I3{}); break;
+            case 4: epilogue_loop(I2{}, I0{}); break;
+            case 5: epilogue_loop(I2{}, I1{}); break;
+            case 6: epilogue_loop(I2{}, I2{}); break;
+            default: epilogue_loop(I2{}, I3{}); break;
         }
     }
 
@@ -1097,13 +1154,17 @@ namespace {
 // tn rows; false if it does not fit.
 struct Geometry {
     int stages, sf_slots, acc_bufs;
+    int stg_bufs;  // TMA-store staging buffers per epilogue warp (0: none fit)
     uint32_t sf_col0;
-    uint32_t off_b, off_sfa, off_sfb, off_bar, b_stage, smem_bytes;
+    uint32_t off_b, off_sfa, off_sfb, off_stg, off_bar, b_stage, smem_bytes;
 };
 
 // TMEM: one or two accumulators of tn columns, then the scale-factor slots.
 // Two accumulators when they fit beside one slot per stage (tn <= 224 with
-// 6-7 stages), else one with as many slots as fit (at least 2).
+// 6-7 stages), else one with as many slots as fit (at least 2). Shared
+// memory: as many operand stages as fit (each one measured worth 5-8% at
+// 4-5 stages), then, only in what is left, one or two 2 KB staging buffers per
+// epilogue warp for the TMA-store epilogue.
 bool geometry(int tn, Geometry* g) {
     const int nblk = (tn + 127) / 128;
     const uint32_t b_stage = static_cast<uint32_t>(tn / 2) * BK;  // multiple of 1024 (tn % 16 == 0)
@@ -1124,8 +1185,17 @@ bool geometry(int tn, Geometry* g) {
     g->off_b = static_cast<uint32_t>(stages) * A_STAGE;
     g->off_sfa = g->off_b + stages * b_stage;
     g->off_sfb = g->off_sfa + stages * SF_ATOM;
-    g->off_bar = g->off_sfb + stages * nblk * SF_ATOM;
-    g->smem_bytes = g->off_bar + 8 * (2 * stages + 5) + 16 + 1024;
+    const uint32_t sf_end = g->off_sfb + stages * nblk * SF_ATOM;
+    const uint32_t bars = 8 * (2 * stages + 5) + 16 + 1024;  // barriers, flag, TMEM slot, base alignment slack
+    g->off_stg = (sf_end + 1023u) & ~1023u;
+    g->stg_bufs = 0;
+    for (int nb = 2; nb >= 1; --nb)
+        if (g->off_stg + nb * EPI_WARPS * STG_CHUNK + bars <= static_cast<uint32_t>(MAIN_SMEM_MAX)) {
+            g->stg_bufs = nb;
+            break;
+        }
+    g->off_bar = g->stg_bufs ? g->off_stg + g->stg_bufs * EPI_WARPS * STG_CHUNK : sf_end;
+    g->smem_bytes = g->off_bar + bars;
     return g->smem_bytes <= static_cast<uint32_t>(MAIN_SMEM_MAX);
 }
 
@@ -1306,6 +1376,7 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     mp.K = a.K;
     mp.ts_max = L.ts_max;
     mp.tiles_m = tc.tiles_m;
+    mp.tma_store = a.tma_store;
     mp.wide_stores = (!tc.kn && tc.tn % 32 == 0 && a.K % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;
     mp.wait_ns = a.wait_limit_ns;
     mp.stall_first_stage = a.stall_first_stage;
@@ -1352,6 +1423,10 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     mp.off_sfa = geo.off_sfa;
     mp.off_sfb = geo.off_sfb;
     mp.off_bar = geo.off_bar;
+    mp.off_stg = geo.off_stg;
+    mp.stg_bufs = geo.stg_bufs;
+    // the caller asks for TMA stores (output map built); they run where staging fits
+    mp.tma_store = (mp.tma_store && geo.stg_bufs > 0 && !tc.kn) ? 1 : 0;
     mp.b_stage = geo.b_stage;
     const int pairs = static_cast<int>(items < max_pairs[dev] ? (items > 0 ? items : 1) : max_pairs[dev]);
     if (ev_before) {
@@ -1371,7 +1446,7 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], maps[4], mp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], mp);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1517,6 +1592,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap* maps, const char**
     mp.K = a.K;
     mp.ts_max = 0;
     mp.tiles_m = 0;
+    mp.tma_store = a.tma_store;
     mp.wide_stores = (tc.tn % 32 == 0 && a.N % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;
     mp.wait_ns = a.wait_limit_ns;
     mp.stall_first_stage = 0;

@@ -237,3 +237,15 @@ def test_grouped_gemm_tile_choice(lib):
                 mx.grouped_gemm_tile_config(*bad)
     finally:
         mx.set_tile_rows(0)
+
+
+def test_epilogue_store_setting(lib):
+    """The epilogue store mode is a validated process-wide setting (host only)."""
+    try:
+        mx.set_epilogue_store(1)
+        mx.set_epilogue_store(0)
+        for bad in (-1, 2):
+            with pytest.raises(mx.Mxfp8Error):
+                mx.set_epilogue_store(bad)
+    finally:
+        mx.set_epilogue_store(0)

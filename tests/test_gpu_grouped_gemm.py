@@ -95,11 +95,14 @@ def test_grouped_gemm_tilings_and_reproducible():
     offs = np.array([250, 251, 777], np.int32)
     outs = []
     try:
-        for tn in (0, 128, 224, 256, 416, 448):
+        for tn in (0, 128, 224, 256, 320, 352, 416, 448):
             mx.set_tile_rows(tn)
-            outs.append(run(X, sX, W, sW, offs))
+            for store in (0, 1):  # TMA stores where their staging fits / direct stores
+                mx.set_epilogue_store(store)
+                outs.append(run(X, sX, W, sW, offs))
     finally:
         mx.set_tile_rows(0)
+        mx.set_epilogue_store(0)
     outs.append(run(X, sX, W, sW, offs))
     for o in outs[1:]:
         assert np.array_equal(outs[0], o)

@@ -256,11 +256,15 @@ def tiling_reset():
     yield
     mx.set_tile_orientation(0)
     mx.set_tile_rows(0)
+    mx.set_epilogue_store(0)
 
 
 # (orientation mode, forced tile rows): the model's choice per orientation,
 # one-MMA tiles, two-MMA tiles (the second 16 columns wide, or 192), narrow tiles
-TILINGS = [(1, 0), (2, 0), (1, 256), (2, 448), (1, 272), (2, 160), (1, 48)]
+TILINGS = [(1, 0), (2, 0), (1, 256), (2, 448), (1, 272), (2, 160), (1, 48), (1, 320), (1, 352), (1, 448)]
+# epilogue stores: TMA stores through shared memory where their staging fits
+# (tn = 48, 256, 320, 352 with its half-chunk stored directly, 448), direct stores
+STORES = (0, 1)
 
 
 @pytest.mark.parametrize("E,N,K,M,sizes", [
@@ -277,15 +281,18 @@ def test_tilings_bit_identical(E, N, K, M, sizes, tiling_reset):
     A, sA = quantised_operand(N, M, seed=E * 7 + N, stream=0)
     B, sB = quantised_operand(K, M, seed=E * 7 + N, stream=1)
     offs = np.cumsum(sizes).astype(np.int32)
-    outs = []
+    outs, names = [], []
     for mode, tn in TILINGS:
         mx.set_tile_orientation(mode)
         mx.set_tile_rows(tn)
         cfg = mx.tile_config(E, N, K, M)
         assert cfg["kn"] == mode - 1 and (tn == 0 or cfg["tn"] == tn)
-        outs.append(run_gpu(A, sA, B, sB, offs, E, N, K))
-    for (mode, tn), o in zip(TILINGS[1:], outs[1:]):
-        assert np.array_equal(outs[0], o), f"tiling mode={mode} tn={tn} differs"
+        for store in STORES:
+            mx.set_epilogue_store(store)
+            outs.append(run_gpu(A, sA, B, sB, offs, E, N, K))
+            names.append(f"mode={mode} tn={tn} store={store}")
+    for name, o in zip(names[1:], outs[1:]):
+        assert np.array_equal(outs[0], o), f"tiling {name} differs"
     check_tol(outs[0], A, sA, B, sB, offs, E, N, K, M)
 
 
@@ -304,8 +311,10 @@ def test_tilings_exact_integers(tiling_reset):
     for mode, tn in TILINGS:
         mx.set_tile_orientation(mode)
         mx.set_tile_rows(tn)
-        got = run_gpu(A, sA, B, sB, offs, E, N, K)
-        assert same_bits_signless_zero(got, ref), f"tiling mode={mode} tn={tn}"
+        for store in STORES:
+            mx.set_epilogue_store(store)
+            got = run_gpu(A, sA, B, sB, offs, E, N, K)
+            assert same_bits_signless_zero(got, ref), f"tiling mode={mode} tn={tn} store={store}"
 
 
 # ------------------------------------------------------------------ extremes of the plan
