@@ -1238,7 +1238,8 @@ TileConfig make_config(int kn, int tn, int rows_m, int rows_n) {
 // rest); W is the output-write floor of a short tile (its 256 x tn bf16
 // stores: about 6.6 K-steps with 32-byte stores, 13 with 16-byte ones, 17 for
 // the transposed 4-byte stores of the 256 side on B), 205 a fixed per-tile
-// cost. The 256 side on B also measured about 8% slower on long tiles.
+// cost; widths whose TMA-store staging fits and whose chunks are all staged
+// (tn % 64 == 0) have the floor 3.7 tn + 815 instead. The 256 side on B also measured about 8% slower on long tiles.
 TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, bool wide_ok, double* cost) {
     TileConfig best{};
     double best_cost = -1.0;
@@ -1250,7 +1251,14 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, b
         const bool wide = !kn && wide_ok && tn % 32 == 0;
         const double w_floor = kn ? 17.0 : (wide ? 6.6 : 13.0);
         const double run = (steps + (g.acc_bufs == 1 && tn > 256 ? 3.0 : 0.0)) * tn * column_cost(tn) * (kn ? 1.08 : 1.0);
-        const double per_tile = (run > w_floor * tn ? run : w_floor * tn) + 205.0;
+        double per_tile = (run > w_floor * tn ? run : w_floor * tn) + 205.0;
+        if (!kn && g.stg_bufs > 0 && tn % 64 == 0) {
+            // TMA-store epilogue with every 32-column chunk staged: a short tile
+            // is bound by 3.7 K-steps per column plus a fixed 815 (measured at
+            // 1-2 K-steps per tile, E = 160 and 512)
+            const double floor_tma = 3.7 * tn + 815.0;
+            per_tile = run + 205.0 > floor_tma ? run + 205.0 : floor_tma;
+        }
         const double c = static_cast<double>(tc.tiles_m) * tc.tiles_n * per_tile;
         if (best_cost < 0 || c < best_cost * (1.0 - 1e-9)) {
             best_cost = c;
@@ -1463,19 +1471,22 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
 
 // Measured cost of one tile of the grouped GEMM (row tiles of 256, a short
 // contraction of K/128 steps: 11-56 on the expert shapes), in microseconds
-// at about 1.9 GHz: a fixed hand-over part a(tn) and b(tn) per K-step, fitted
-// on GB300 over the forward and data-gradient products of the 16B and 671B
-// expert layers (tn = 128 .. 448 with 32-byte output stores where tn % 32 ==
-// 0). With one accumulator every tile waits for the previous tile's TMEM
-// drain, which short tiles do not amortise; widths of 16 mod 32 store in
-// 16-byte pieces, part of which falls inside that wait.
+// at about 1.9-2.0 GHz: a fixed hand-over part a(tn) and b(tn) per K-step,
+// fitted on GB300 over the forward and data-gradient products of the 16B and
+// 671B expert layers (tn = 128 .. 448, each with its default epilogue: TMA
+// stores where their staging fits beside the operand ring, e.g. tn = 256,
+// 352, 448, else 32-byte register stores where tn % 32 == 0). With one
+// accumulator every tile waits for the previous tile's TMEM drain, which
+// short tiles do not amortise; tn = 256 (one MMA per 32-element chunk, six
+// stages, staged stores) measured best on most shapes; widths of 16 mod 32
+// store in 16-byte pieces, part of which falls inside that wait.
 double gemm_tile_cost(int tn, bool wide_ok, double steps) {
     static const double ab[][2] = {
         // tn = 128, 144, ..., 448
-        {1.02, 0.318}, {1.13, 0.322}, {1.00, 0.329}, {1.39, 0.338}, {0.93, 0.344}, {1.57, 0.359},
-        {1.57, 0.361}, {2.06, 0.382}, {1.19, 0.419}, {4.66, 0.487}, {3.16, 0.477}, {5.28, 0.476},
-        {2.86, 0.506}, {4.89, 0.498}, {3.23, 0.519}, {5.12, 0.532}, {3.12, 0.539}, {5.25, 0.553},
-        {2.46, 0.624}, {4.61, 0.638}, {2.87, 0.630}};
+        {1.09, 0.318}, {1.37, 0.316}, {1.25, 0.321}, {1.28, 0.333}, {1.09, 0.341}, {2.30, 0.340},
+        {1.82, 0.360}, {1.64, 0.370}, {1.88, 0.346}, {4.72, 0.474}, {3.28, 0.466}, {5.44, 0.471},
+        {2.91, 0.473}, {2.63, 0.520}, {2.84, 0.525}, {2.86, 0.546}, {3.36, 0.529}, {5.27, 0.565},
+        {3.00, 0.584}, {2.80, 0.598}, {2.25, 0.624}};
     if (tn < 128) {
         // narrower than measured: the long-tile column cost, scaled from tn = 128
         const double b = ab[0][1] * (tn * column_cost(tn)) / (128.0 * column_cost(128));

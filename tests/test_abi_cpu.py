@@ -114,8 +114,9 @@ def test_tile_config_choice(lib):
         assert mx.tile_config(32, 4096, 7168, 262144) == {"kn": 0, "tn": 448, "tiles_m": 16, "tiles_n": 16}
         # 671B down: K = 2048 in 5 tiles of 416 (1.6% padding), the 256 side on A (N = 7168)
         assert mx.tile_config(32, 7168, 2048, 524288) == {"kn": 0, "tn": 416, "tiles_m": 28, "tiles_n": 5}
-        # many experts with 32 tokens each: bound by writing the output, widest tiles
-        assert mx.tile_config(512, 512, 2048, 16384) == {"kn": 0, "tn": 416, "tiles_m": 2, "tiles_n": 5}
+        # many experts with 32 tokens each: bound by writing the output; the widest
+        # tiles whose chunks are all written by staged TMA stores
+        assert mx.tile_config(512, 512, 2048, 16384) == {"kn": 0, "tn": 448, "tiles_m": 2, "tiles_n": 5}
         mx.set_tile_orientation(2)
         assert mx.tile_config(8, 1408, 2048, 32768)["kn"] == 1
         mx.set_tile_orientation(1)
@@ -217,16 +218,16 @@ def test_grouped_gemm_tile_choice(lib):
     is honoured; sizes the entry point rejects fail."""
     try:
         mx.set_tile_rows(0)
-        # 16B forward (hidden 2048 -> 1408): 4 tiles of 352, 32-byte stores
-        assert mx.grouped_gemm_tile_config(8, 1408, 2048, 32768) == {"tn": 352, "tiles_m_max": 136, "tiles_n": 4}
+        # 16B forward (hidden 2048 -> 1408): 6 tiles of 256 (one MMA per chunk, staged TMA stores)
+        assert mx.grouped_gemm_tile_config(8, 1408, 2048, 32768) == {"tn": 256, "tiles_m_max": 136, "tiles_n": 6}
         # 16B data gradient (1408 -> 2048, 11 K-steps): one 256-wide MMA per chunk
         assert mx.grouped_gemm_tile_config(8, 2048, 1408, 32768) == {"tn": 256, "tiles_m_max": 136, "tiles_n": 8}
         # 671B up/gate forward (7168 -> 4096) and data gradient (4096 -> 7168)
-        assert mx.grouped_gemm_tile_config(32, 4096, 7168, 262144)["tn"] == 384
+        assert mx.grouped_gemm_tile_config(32, 4096, 7168, 262144)["tn"] == 256
         assert mx.grouped_gemm_tile_config(32, 7168, 4096, 262144)["tn"] == 448
         # 671B down forward (2048 -> 7168) and data gradient (7168 -> 2048)
         assert mx.grouped_gemm_tile_config(32, 7168, 2048, 524288) == {"tn": 448, "tiles_m_max": 2080, "tiles_n": 16}
-        assert mx.grouped_gemm_tile_config(32, 2048, 7168, 524288)["tn"] == 416
+        assert mx.grouped_gemm_tile_config(32, 2048, 7168, 524288)["tn"] == 256
         # narrow outputs: one column tile
         assert mx.grouped_gemm_tile_config(16, 64, 128, 900) == {"tn": 64, "tiles_m_max": 20, "tiles_n": 1}
         mx.set_tile_rows(224)
