@@ -52,7 +52,9 @@ class L2Flush:
         import torch
 
         self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+        # float32: the sum is one reduction kernel that only reads (an integer
+        # sum would first widen the buffer into a temporary, i.e. write again)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     def __call__(self):
         self.w.zero_()
