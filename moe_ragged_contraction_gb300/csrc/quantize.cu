@@ -85,29 +85,37 @@ __global__ void __launch_bounds__(QT_THREADS) quantize_tokenwise_kernel(const fl
 // Quantise-and-transpose from token-major bf16: x [M][R] (the layout dY and X
 // have in the forward and backward passes) to q [R][M] E4M3 with the token
 // axis contiguous and s [R][M/32], by the same rule as above (bf16 values are
-// exact in fp32). A block handles 128 tokens x 128 features. Each thread
-// loads an 8-token x 8-feature sub-block (eight 16-byte row pieces),
-// transposes it in registers with byte permutes and writes eight 16-byte
-// feature pieces into shared memory (rows of 136 bf16: 272 bytes, so the
-// 16-byte reads below are free of bank conflicts); then each thread
-// quantises two (feature, 32-token block) pairs, writing each block's 32
-// bytes as one full sector.
+// exact in fp32). A block handles a tile of 128 tokens x 128 features in two
+// phases, each laid out so that a warp's memory instruction touches few
+// cache lines (the L1 pipeline, not DRAM, limited the first version):
+//  * load + transpose: thread (fg = lane % 16, tg = 2 warp + lane / 16) loads
+//    the 8 x 8 sub-block of tokens 8 tg .. +7 and features 8 fg .. +7 (one
+//    16-byte piece per token: a warp's load covers two whole 256-byte token
+//    rows), transposes it in registers with byte permutes and writes eight
+//    16-byte pieces (feature rows 8 fg + j, piece tg) into shared memory;
+//  * quantise: in each of two passes, thread (feature 16 warp + 8 pass +
+//    lane % 8, 32-token block lane / 8) reads its 32 values, finds the block's
+//    exponent and writes 32 E4M3 bytes and the scale byte: a warp's store
+//    covers 8 features x 128 contiguous bytes.
+// Shared rows are 256 bytes, 16-byte piece p of row r stored at piece
+// p ^ (r % 8) ^ (r / 8 % 8): the eight lanes of each 16-byte access phase then
+// hit eight different bank groups in both phases.
 constexpr int QX_TOK = 128;
 constexpr int QX_FEAT = 128;
 constexpr int QX_THREADS = 256;
-constexpr int QX_ROW = 136;  // padded shared row (bf16 elements)
+
+__device__ __forceinline__ int qx_piece(int row, int p) { return p ^ (row & 7) ^ ((row >> 3) & 7); }
 
 __global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(const uint16_t* __restrict__ x,
                                                                              long long M, int R, int vec,
                                                                              uint8_t* __restrict__ q,
                                                                              uint8_t* __restrict__ s) {
-    extern __shared__ __align__(16) uint16_t sT[];  // [QX_FEAT][QX_ROW]
+    extern __shared__ __align__(16) uint4 sT[];  // [QX_FEAT][16] pieces of 8 bf16 (tokens)
     const long long t0 = static_cast<long long>(blockIdx.x) * QX_TOK;
     const int f0 = blockIdx.y * QX_FEAT;
-    const int tid = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     {
-        // thread -> tokens t0 + 8 tg .. +7, features f0 + 8 fg .. +7
-        const int tg = tid & 15, fg = tid >> 4;
+        const int fg = lane & 15, tg = 2 * warp + (lane >> 4);
         const int fb = f0 + 8 * fg;
         uint32_t r[8][4];  // r[i][w]: features (2w, 2w+1) of token i
 #pragma unroll
@@ -135,25 +143,24 @@ __global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(con
             c.y = __byte_perm(r[2][j >> 1], r[3][j >> 1], sel);
             c.z = __byte_perm(r[4][j >> 1], r[5][j >> 1], sel);
             c.w = __byte_perm(r[6][j >> 1], r[7][j >> 1], sel);
-            *reinterpret_cast<uint4*>(sT + (8 * fg + j) * QX_ROW + 8 * tg) = c;
+            const int row = 8 * fg + j;
+            sT[row * 16 + qx_piece(row, tg)] = c;
         }
     }
     __syncthreads();
-    // thread -> feature f0 + (tid % 128), token blocks 2 (tid / 128) and 2 (tid / 128) + 1
-    const int fl = tid & (QX_FEAT - 1);
-    const int f = f0 + fl;
-    if (f >= R) return;
+    const int b = lane >> 3;                    // 32-token block of the tile
+    const long long tb = t0 + 32 * b;           // its first token
+    if (tb >= M) return;                        // M % 32 == 0: a block is all in or all out
 #pragma unroll 1
-    for (int bb = 0; bb < 2; ++bb) {
-        const int b = 2 * (tid >> 7) + bb;
-        const long long tb = t0 + 32 * b;  // first token of the block
-        if (tb >= M) return;               // M % 32 == 0: a block is all in or all out
+    for (int pass = 0; pass < 2; ++pass) {
+        const int fl = 16 * warp + 8 * pass + (lane & 7);
+        const int f = f0 + fl;
+        if (f >= R) continue;
         float v[32];
         uint32_t amax_bits = 0;
-        const uint4* row = reinterpret_cast<const uint4*>(sT + fl * QX_ROW + 32 * b);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint4 w = row[i];
+            const uint4 w = sT[fl * 16 + qx_piece(fl, 4 * b + i)];
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -204,7 +211,7 @@ cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8
     const long long gx = (M + QX_TOK - 1) / QX_TOK;
     const int gy = (R + QX_FEAT - 1) / QX_FEAT;
     if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
-    constexpr size_t smem = sizeof(uint16_t) * QX_FEAT * QX_ROW;  // 34 KB
+    constexpr size_t smem = sizeof(uint16_t) * QX_FEAT * QX_TOK;  // 32 KB
     quantize_transpose_bf16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), QX_THREADS, smem,
                                      stream>>>(x, M, R, vec, q, s);
     return cudaGetLastError();
