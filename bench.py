@@ -498,7 +498,8 @@ def bench_quantizer(args):
 
     import moe_ragged_contraction_gb300 as mx
 
-    device = torch.device("cuda")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
     mx.build()
     mx.load()
     w = I.WORKLOADS[args.config]
@@ -516,6 +517,9 @@ def bench_quantizer(args):
         mx.quantize_transpose_bf16(dy, qa, sa)
         mx.quantize_transpose_bf16(x, qb, sb)
 
+    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(device).uuid))
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         flush()
         step()
@@ -530,6 +534,7 @@ def bench_quantizer(args):
         ev[i][1].record()
     torch.cuda.synchronize()
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    clocks = sampler.stop()
     elems = float(w.M) * (w.N + w.K)
     alg = elems * (2 + 1 + 1 / 32)
     _, _, peaks = mxfp8_peak()
@@ -541,7 +546,7 @@ def bench_quantizer(args):
                        "l2": L2Flush.DESCRIPTION},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "algorithmic_bytes_per_step": alg, "kernel": "quantize_transpose_bf16_kernel"},
-            "gpu_launches": 2 * K}
+            "gpu_launches": 2 * K, "clocks": clocks}
 
 
 # ------------------------------------------------------------------ grouped GEMM (forward / data gradient)
