@@ -62,9 +62,12 @@ class L2Flush:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources that define the main kernel, its prep kernels and
+    their host-side setup (the quantisers are not part of it)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.dirname(MAIN_KERNEL_SRC))):
-        with open(os.path.join(os.path.dirname(MAIN_KERNEL_SRC), f), "rb") as fh:
+    d = os.path.dirname(MAIN_KERNEL_SRC)
+    for f in ("abi.cu", "mxw_internal.h", "mxw_ptx.cuh", "wgrad_kernels.cu"):
+        with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
