@@ -135,3 +135,33 @@ def test_grouped_gemm_16B_expert_shape_sampled():
     got = out.view(torch.int16)[torch.from_numpy(t).cuda(), torch.from_numpy(n).cuda()].cpu().numpy().view(np.uint16)
     bad = tolerance_violations(got, ref, aacc)
     assert not bad.any(), f"{bad.sum()} of {bad.size} sampled elements out of tolerance"
+
+
+@pytest.mark.parametrize("E,M,N,K,sizes", [
+    (3, 64, 256, 64, [0, 0, 0]),          # every group empty: the whole output is padding
+    (1, 1, 32, 32, [1]),                  # one row, one partial K-step (one k = 32 MMA)
+    (2, 160, 8, 160, [150, 10]),          # the narrowest output (N = 8), K-step of 32 + partial
+    (5, 2000, 264, 96, None),             # M not a multiple of 32, random group boundaries
+    (2, 512, 1408, 2048, [511, 1]),       # a one-row group after a 511-row group
+])
+def test_grouped_gemm_edge_shapes(E, M, N, K, sizes):
+    rng = np.random.default_rng(E * 7 + M + N + K)
+    if sizes is None:
+        offs = np.sort(rng.integers(0, M + 1, E)).astype(np.int32)
+    else:
+        offs = np.cumsum(sizes).astype(np.int32)
+    X, sX = quantised_operand(M, K, seed=M + K, stream=0)
+    W, sW = weights(E, N, K, seed=M + K)
+    outs = []
+    try:
+        for store in (0, 1):
+            mx.set_epilogue_store(store)
+            outs.append(run(X, sX, W, sW, offs))
+    finally:
+        mx.set_epilogue_store(0)
+    assert np.array_equal(outs[0], outs[1])
+    assert mx.device_status(clear=True) == 0
+    ref, _, aacc = oracle.grouped_gemm(X, sX, W, sW, offs, E, M, N, K, want_acc=True)
+    bad = tolerance_violations(outs[0], ref, aacc)
+    assert not bad.any(), f"{bad.sum()} of {bad.size} out of tolerance"
+    assert np.all(outs[0][int(offs[-1]):] == 0), "padding rows not +0"
