@@ -323,27 +323,51 @@ def bench_gpu(args):
     main_ms = [a.elapsed_time(b) for a, b in evm]
     assert mx.device_status(clear=True) == 0, "device flagged an error during the benchmark"
 
-    # end to end through the public API with host buffers: H2D of every input,
-    # the call, D2H of the output, all inside the timed interval
+    # end to end through the public API with host buffers: every step copies its
+    # inputs host -> device (pinned host memory) and its result device -> host
+    # inside the timed interval. Consecutive steps overlap like a streaming
+    # pipeline: the copy-in of step i+1, the call of step i and the copy-out of
+    # step i-1 run on three streams over two device buffer sets, ordered by
+    # events (a set's inputs are overwritten only after its call finished, its
+    # output only after it was copied out).
     hA, hsA, hB, hsB, hoffs = (t.cpu().pin_memory() for t in (A, sA, B, sB, offs))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB, hoffs))
     d2h = hout.numel() * hout.element_size()
-    dA, dsA, dB, dsB, doffs = (torch.empty_like(t) for t in (A, sA, B, sB, offs))
+    sets = [tuple(torch.empty_like(t) for t in (A, sA, B, sB, offs, out)) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # the set's inputs have landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the set's call has finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # the set's output has been copied out
 
-    def e2e_step():
-        for d, h in ((dA, hA), (dsA, hsA), (dB, hB), (dsB, hsB), (doffs, hoffs)):
-            d.copy_(h, non_blocking=True)
-        mx.wgrad_grouped(dA, dsA, dB, dsB, doffs, out=out)
-        hout.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        dA, dsA, dB, dsB, doffs, dout = sets[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_used[b])
+            for d, h in ((dA, hA), (dsA, hsA), (dB, hB), (dsB, hsB), (doffs, hoffs)):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])
+        mx.wgrad_grouped(dA, dsA, dB, dsB, doffs, out=dout, stream=stream)
+        ev_used[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_used[b])
+            hout.copy_(dout, non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
+    for i in range(max(3, args.warmup)):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K):
-        e2e_step()
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    for i in range(K):
+        e2e_step(i)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
@@ -401,7 +425,9 @@ def bench_gpu(args):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "pipelining": "copy-in, call and copy-out of consecutive steps overlap (three streams, "
+                                  "two device buffer sets)"},
             "gpu_launches": 2 * K,
             "clocks": clocks,
         }
