@@ -279,6 +279,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a0, uint32_
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads of them (a TMA store issued after a warp barrier).
 __device__ __forceinline__ void fence_proxy_async_shared() {

@@ -555,7 +555,7 @@ struct MainParams {
     int stages, sf_slots;
     int acc_bufs;            // accumulators in TMEM (2: the next tile's MMAs overlap this tile's drain)
     int wide_stores;         // 32-byte output stores (rows of 16 columns 32-byte aligned), else 16-byte
-    int tma_store;           // epilogue chunks through shared memory and TMA stores (rows of A on the 256 side)
+    int tma_store;           // epilogue chunks through shared memory and TMA stores (transposed tiles: weight gradient only)
     int stg_bufs;            // staging buffers per epilogue warp (1 or 2) when tma_store
     uint32_t sf_col0;        // first TMEM column of the scale-factor slots
     uint32_t off_b, off_sfa, off_sfb, off_stg, off_bar, b_stage;  // shared-memory layout (bytes)
@@ -970,7 +970,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         auto epilogue_loop = [&](auto nbuf_tag, auto mode_tag) {
             constexpr uint32_t BUF_SHIFT = decltype(nbuf_tag)::value == 2 ? 1u : 0u;
             // 0: rows of A on the 256 side, 16-byte stores; 1: the same with
-            // 32-byte stores; 2: rows of B on the 256 side (transposed stores);
+            // 32-byte stores; 2: rows of B on the 256 side (transposed: 4-byte
+            // stores, or TMA stores through shared memory when p.tma_store);
             // 3: rows of A on the 256 side through shared memory and TMA stores
             constexpr int MODE = decltype(mode_tag)::value;
             uint32_t ntile = 0;  // non-empty tiles drained so far
@@ -1000,6 +1001,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                 // lane stores (k, k+1) of row n and the odd lane (k, k+1) of row
                 // n+1: 4-byte stores, 64 contiguous bytes per row and instruction.
                 auto store_chunk = [&](int j, const uint32_t (&v)[32]) {
+                    if (MODE == 2 && p.tma_store) {
+                        // transposed tile through a staging buffer: the chunk is
+                        // output rows n = ncol0 + 32 j .. + 31 (TMEM columns) by
+                        // columns k = the warp's 32 lanes; after the pair exchange
+                        // below, the even lane holds (k, k + 1) of row n and the odd
+                        // lane those of row n + 1. Staged as 32 rows (n) x 64 bytes
+                        // with the 64-byte swizzle: one 4-byte store per lane and
+                        // column pair, rows n and n + 1 in different bank halves
+                        const int k0w = it.m0 + static_cast<int>(rank) * BM + q * 32;
+                        if (32 * j + 32 <= ncols && k0w < p.K && ncol0 + 32 * j < p.N) {
+                            if (lane == 0) {
+                                if (p.stg_bufs == 2) bulk_wait_group_read<1>();
+                                else bulk_wait_group_read<0>();
+                            }
+                            __syncwarp();
+                            const uint32_t buf = stg_warp + sbuf * STG_CHUNK;
+                            const uint32_t kb = static_cast<uint32_t>(lane & ~1) * 2u;  // byte of k2 in the row
+#pragma unroll
+                            for (int c = 0; c < 32; c += 2) {
+                                const uint32_t mine = pack_bf16x2(v[c], v[c + 1]);
+                                const uint32_t got = __shfl_xor_sync(0xffffffffu, mine, 1);
+                                const uint32_t w =
+                                    odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
+                                const uint32_t r = static_cast<uint32_t>(c) + (odd ? 1u : 0u);
+                                const uint32_t piece = (kb >> 4) ^ ((r >> 1) & 3u);
+                                st_shared_b32(buf + r * 64u + piece * 16u + (kb & 15u), w);
+                            }
+                            fence_proxy_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&tmOut, buf, k0w, ncol0 + 32 * j, it.g);
+                                bulk_commit_group();
+                            }
+                            sbuf ^= static_cast<uint32_t>(p.stg_bufs - 1);
+                            return;
+                        }
+                        // a partial chunk: the 4-byte stores below
+                    }
                     if (MODE == 3) {
                         // whole 32 x 32 chunks (inside this warp's columns and, for
                         // ragged rows, inside the group) go through a staging buffer:
@@ -1116,7 +1155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                 }
                 ++ntile;
             }
-            if (MODE == 3) {
+            if (MODE == 3 || (MODE == 2 && p.tma_store)) {
                 // every TMA store of this warp has completed before the CTA may exit
                 if (lane == 0) bulk_wait_group_all();
                 __syncwarp();
@@ -1205,13 +1244,15 @@ bool geometry(int tn, Geometry* g) {
 // up/gate and down expert shapes with the 256 side on A). Narrow tiles pay the
 // per-step scale-factor copies and the M-side operand bytes over fewer
 // columns; tn just above 256 adds a second MMA too narrow to run at full
-// rate; around 384-448 the operand bytes per column are lowest.
+// rate; around 384-448 the operand bytes per column are lowest. The entry
+// for 352 comes from the 16B expert shape instead (tn = 352 against 416 with
+// the 256 side on A, at 4096 and 24576 tokens per expert: 0.917-0.92).
 double column_cost(int tn) {
     static const double f[] = {
         // tn = 16, 32, ..., 448
-        3.00, 2.60, 2.30, 2.00, 1.85, 1.70, 1.60, 1.49,          // 16 .. 128
-        1.28, 1.175, 1.14, 1.063, 1.063, 1.002, 0.985, 1.00,     // 144 .. 256
-        1.094, 1.039, 1.066, 1.023, 0.982, 0.979, 0.948, 0.914,  // 272 .. 384
+        3.00, 2.60, 2.30, 2.00, 1.85, 1.70, 1.60, 1.49,         // 16 .. 128
+        1.28, 1.175, 1.14, 1.063, 1.063, 1.002, 0.985, 1.00,    // 144 .. 256
+        1.094, 1.039, 1.066, 1.023, 0.982, 0.92, 0.948, 0.914,  // 272 .. 384
         0.919, 0.89, 0.912, 0.902};                             // 400 .. 448
     return f[tn / 16 - 1];
 }
@@ -1239,7 +1280,11 @@ TileConfig make_config(int kn, int tn, int rows_m, int rows_n) {
 // stores: about 6.6 K-steps with 32-byte stores, 13 with 16-byte ones, 17 for
 // the transposed 4-byte stores of the 256 side on B), 205 a fixed per-tile
 // cost; widths whose TMA-store staging fits and whose chunks are all staged
-// (tn % 64 == 0) have the floor 3.7 tn + 815 instead. The 256 side on B also measured about 8% slower on long tiles.
+// (tn % 64 == 0) have the floor 3.7 tn + 815 instead. The 256 side on B also
+// measured about 8% slower on long tiles with its 4-byte register stores and
+// about 4% slower where its chunks go through TMA stores (the 16B and 671B
+// down expert shapes: tn = 352 and 448 against 416 on A, weighed with the
+// column costs above).
 TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, bool wide_ok, double* cost) {
     TileConfig best{};
     double best_cost = -1.0;
@@ -1250,7 +1295,8 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, b
         const TileConfig tc = make_config(kn, tn, rows_m, rows_n);
         const bool wide = !kn && wide_ok && tn % 32 == 0;
         const double w_floor = kn ? 17.0 : (wide ? 6.6 : 13.0);
-        const double run = (steps + (g.acc_bufs == 1 && tn > 256 ? 3.0 : 0.0)) * tn * column_cost(tn) * (kn ? 1.08 : 1.0);
+        const double kn_factor = g.stg_bufs > 0 ? 1.04 : 1.08;
+        const double run = (steps + (g.acc_bufs == 1 && tn > 256 ? 3.0 : 0.0)) * tn * column_cost(tn) * (kn ? kn_factor : 1.0);
         double per_tile = (run > w_floor * tn ? run : w_floor * tn) + 205.0;
         if (!kn && g.stg_bufs > 0 && tn % 64 == 0) {
             // TMA-store epilogue with every 32-column chunk staged: a short tile
@@ -1434,7 +1480,7 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     mp.off_stg = geo.off_stg;
     mp.stg_bufs = geo.stg_bufs;
     // the caller asks for TMA stores (output map built); they run where staging fits
-    mp.tma_store = (mp.tma_store && geo.stg_bufs > 0 && !tc.kn) ? 1 : 0;
+    mp.tma_store = (mp.tma_store && geo.stg_bufs > 0 && (!tc.kn || mp.mode == 0)) ? 1 : 0;
     mp.b_stage = geo.b_stage;
     const int pairs = static_cast<int>(items < max_pairs[dev] ? (items > 0 ? items : 1) : max_pairs[dev]);
     if (ev_before) {

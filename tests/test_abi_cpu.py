@@ -108,8 +108,10 @@ def test_tile_config_choice(lib):
     try:
         mx.set_tile_orientation(0)
         mx.set_tile_rows(0)
-        # 16B expert shape: K = 2048 in 5 tiles of 416 (two MMAs, 32-byte stores), N = 1408 on the 256 side
-        assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 0, "tn": 416, "tiles_m": 6, "tiles_n": 5}
+        # 16B expert shape: K = 2048 = 8 x 256 on the 256 side (B), N = 1408 = 4 x 352
+        # (two MMAs, TMA stores of the transposed chunks): no padding on either side
+        assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 1, "tn": 352, "tiles_m": 8, "tiles_n": 4}
+        assert mx.tile_config(8, 1408, 2048, 196608) == {"kn": 1, "tn": 352, "tiles_m": 8, "tiles_n": 4}
         # 671B up/gate: K = 7168 = 16 x 448 with the 256 side on A (N = 4096)
         assert mx.tile_config(32, 4096, 7168, 262144) == {"kn": 0, "tn": 448, "tiles_m": 16, "tiles_n": 16}
         # 671B down: K = 2048 in 5 tiles of 416 (1.6% padding), the 256 side on A (N = 7168)
@@ -117,9 +119,8 @@ def test_tile_config_choice(lib):
         # many experts with 32 tokens each: bound by writing the output; the widest
         # tiles whose chunks are all written by staged TMA stores
         assert mx.tile_config(512, 512, 2048, 16384) == {"kn": 0, "tn": 448, "tiles_m": 2, "tiles_n": 5}
-        mx.set_tile_orientation(2)
-        assert mx.tile_config(8, 1408, 2048, 32768)["kn"] == 1
         mx.set_tile_orientation(1)
+        assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 0, "tn": 416, "tiles_m": 6, "tiles_n": 5}
         mx.set_tile_rows(256)
         assert mx.tile_config(8, 1408, 2048, 32768) == {"kn": 0, "tn": 256, "tiles_m": 6, "tiles_n": 8}
         mx.set_tile_orientation(2)

@@ -261,9 +261,11 @@ def tiling_reset():
 
 # (orientation mode, forced tile rows): the model's choice per orientation,
 # one-MMA tiles, two-MMA tiles (the second 16 columns wide, or 192), narrow tiles
-TILINGS = [(1, 0), (2, 0), (1, 256), (2, 448), (1, 272), (2, 160), (1, 48), (1, 320), (1, 352), (1, 448)]
+TILINGS = [(1, 0), (2, 0), (1, 256), (2, 448), (1, 272), (2, 160), (1, 48), (1, 320), (1, 352), (1, 448),
+           (2, 352)]
 # epilogue stores: TMA stores through shared memory where their staging fits
-# (tn = 48, 256, 320, 352 with its half-chunk stored directly, 448), direct stores
+# (tn = 48, 256, 320, 352 with its half-chunk stored directly, 448; both
+# orientations), direct stores
 STORES = (0, 1)
 
 
