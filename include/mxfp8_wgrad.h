@@ -259,8 +259,9 @@ int mxfp8_wgrad_tile_config(int E, int N, int K, int64_t M, int* kn, int* tn, in
  * _noalloc} and mxfp8_grouped_gemm): mode 0 (default) narrows each 32 x 32
  * block of the accumulator into a shared-memory staging buffer and writes it
  * with a TMA store, wherever the staging fits beside the operand pipeline
- * without costing a stage (the 256-row side on A, out 16-byte aligned, output
- * rows a multiple of 8 elements); blocks that straddle a tile, group or output
+ * without costing a stage (out 16-byte aligned, output rows a multiple of 8
+ * elements; either orientation of the weight gradient's tiles, the 256-row
+ * side on X in the grouped GEMM); blocks that straddle a tile, group or output
  * edge, and all other tilings, store straight from registers. Mode 1 stores
  * straight from registers always. The results are the same bits either way.
  * The initial mode comes from MXFP8_EPILOGUE_STORE ("auto" or "direct").
