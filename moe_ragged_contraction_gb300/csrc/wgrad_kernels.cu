@@ -957,9 +957,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         // TMEM lane = M-side row of this CTA's half, column = N-side row of the
         // tile. Two warps share each 32-lane quarter, each draining half of the
         // tn columns (at most 224) in 32-column loads: up to four chunks in
-        // flight at once; with more than four, the first four are stored
-        // before the rest is loaded (registers hold 128 columns at most). The
-        // accumulator is released after the last load.
+        // flight at once; with more than four, the remainder (one to three
+        // chunks) is loaded and stored before the last four are loaded
+        // (registers hold 128 columns at most). The accumulator is released
+        // after the last load.
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int h = (warp - EPI_WARP0) >> 2;  // column half of the tile
         const int ncols = p.tn >> 1;
@@ -1139,19 +1140,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                         else mbar_arrive_cluster(tempty_leader + 8 * buf);
                     }
                 };
+                // batches of at most four chunks, the short one first: the
+                // accumulator is released after the last batch's loads, so only
+                // the first batch's stores precede the release
+                const int first = nchunks - 4 * ((nchunks - 1) >> 2);
 #pragma unroll 1
-                for (int j0 = 0; j0 < nchunks; j0 += 4) {
+                for (int j0 = 0, nb = first; j0 < nchunks; j0 += nb, nb = 4) {
                     uint32_t v[4][32];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (j0 + j < nchunks) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
+                        if (j < nb) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-                    if (j0 + 4 >= nchunks) release();
+                    if (j0 + nb >= nchunks) release();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (j0 + j < nchunks) store_chunk(j0 + j, v[j]);
+                        if (j < nb) store_chunk(j0 + j, v[j]);
                 }
                 ++ntile;
             }
