@@ -968,8 +968,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
         // the loop is instantiated per accumulator count (1 or 2), which keeps
         // the buffer index out of the registers the TMEM loads need
-        auto epilogue_loop = [&](auto nbuf_tag, auto mode_tag) {
+        auto epilogue_loop = [&](auto nbuf_tag, auto mode_tag, auto packed_tag) {
             constexpr uint32_t BUF_SHIFT = decltype(nbuf_tag)::value == 2 ? 1u : 0u;
+            // the whole drained row held as bf16 pairs (five or six chunks)
+            constexpr bool PACKED = decltype(packed_tag)::value != 0;
+            constexpr int PACK_CHUNKS = 6;
             // 0: rows of A on the 256 side, 16-byte stores; 1: the same with
             // 32-byte stores; 2: rows of B on the 256 side (transposed: 4-byte
             // stores, or TMA stores through shared memory when p.tma_store);
@@ -1001,7 +1004,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                 // KN: neighbouring lanes swap their (n, n+1) pairs so that the even
                 // lane stores (k, k+1) of row n and the odd lane (k, k+1) of row
                 // n+1: 4-byte stores, 64 contiguous bytes per row and instruction.
-                auto store_chunk = [&](int j, const uint32_t (&v)[32]) {
+                // w(i) gives columns 2i and 2i + 1 of the chunk as a bf16 pair.
+                auto store_chunk = [&](int j, auto w) {
                     if (MODE == 2 && p.tma_store) {
                         // transposed tile through a staging buffer: the chunk is
                         // output rows n = ncol0 + 32 j .. + 31 (TMEM columns) by
@@ -1021,13 +1025,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                             const uint32_t kb = static_cast<uint32_t>(lane & ~1) * 2u;  // byte of k2 in the row
 #pragma unroll
                             for (int c = 0; c < 32; c += 2) {
-                                const uint32_t mine = pack_bf16x2(v[c], v[c + 1]);
+                                const uint32_t mine = w(c >> 1);
                                 const uint32_t got = __shfl_xor_sync(0xffffffffu, mine, 1);
-                                const uint32_t w =
+                                const uint32_t x =
                                     odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
                                 const uint32_t r = static_cast<uint32_t>(c) + (odd ? 1u : 0u);
                                 const uint32_t piece = (kb >> 4) ^ ((r >> 1) & 3u);
-                                st_shared_b32(buf + r * 64u + piece * 16u + (kb & 15u), w);
+                                st_shared_b32(buf + r * 64u + piece * 16u + (kb & 15u), x);
                             }
                             fence_proxy_async_shared();
                             __syncwarp();
@@ -1062,10 +1066,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                             for (int c4 = 0; c4 < 4; ++c4) {
                                 const uint32_t piece = static_cast<uint32_t>(c4) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
                                 st_shared_v4(buf + static_cast<uint32_t>(lane) * 64u + piece * 16u,
-                                             pack_bf16x2(v[8 * c4 + 0], v[8 * c4 + 1]),
-                                             pack_bf16x2(v[8 * c4 + 2], v[8 * c4 + 3]),
-                                             pack_bf16x2(v[8 * c4 + 4], v[8 * c4 + 5]),
-                                             pack_bf16x2(v[8 * c4 + 6], v[8 * c4 + 7]));
+                                             w(4 * c4 + 0), w(4 * c4 + 1), w(4 * c4 + 2), w(4 * c4 + 3));
                             }
                             fence_proxy_async_shared();
                             __syncwarp();
@@ -1084,11 +1085,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                         for (int c = 0; c < 32; c += 16) {
                             const int cc = 32 * j + c;
                             if (row_in && cc < ncols && ncol0 + cc < p.col_limit)
-                                st_global_v8(obase + cc, pack_bf16x2(v[c + 0], v[c + 1]),
-                                             pack_bf16x2(v[c + 2], v[c + 3]), pack_bf16x2(v[c + 4], v[c + 5]),
-                                             pack_bf16x2(v[c + 6], v[c + 7]), pack_bf16x2(v[c + 8], v[c + 9]),
-                                             pack_bf16x2(v[c + 10], v[c + 11]), pack_bf16x2(v[c + 12], v[c + 13]),
-                                             pack_bf16x2(v[c + 14], v[c + 15]));
+                                st_global_v8(obase + cc, w(c / 2 + 0), w(c / 2 + 1), w(c / 2 + 2), w(c / 2 + 3),
+                                             w(c / 2 + 4), w(c / 2 + 5), w(c / 2 + 6), w(c / 2 + 7));
                         }
                     } else if (MODE == 0 || MODE == 3) {
 #pragma unroll
@@ -1096,30 +1094,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                             const int cc = 32 * j + c;
                             if (row_in && cc < ncols && ncol0 + cc < p.col_limit)
                                 *reinterpret_cast<uint4*>(obase + cc) =
-                                    make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
-                                               pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
+                                    make_uint4(w(c / 2 + 0), w(c / 2 + 1), w(c / 2 + 2), w(c / 2 + 3));
                         }
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
                             const int cc = 32 * j + c;
                             if (cc < ncols) {  // the same for the whole warp
-                                const uint32_t mine = pack_bf16x2(v[c], v[c + 1]);
+                                const uint32_t mine = w(c >> 1);
                                 const uint32_t got = __shfl_xor_sync(0xffffffffu, mine, 1);
                                 // even: (own n, partner n) = row n; odd: (partner n+1, own n+1) = row n+1
-                                const uint32_t w = odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
+                                const uint32_t x = odd ? __byte_perm(got, mine, 0x7632) : __byte_perm(mine, got, 0x5410);
                                 const int n = ncol0 + cc + (odd ? 1 : 0);
-                                if (row_in && n < p.N) *reinterpret_cast<uint32_t*>(obase + static_cast<size_t>(n) * p.K) = w;
+                                if (row_in && n < p.N) *reinterpret_cast<uint32_t*>(obase + static_cast<size_t>(n) * p.K) = x;
                             }
                         }
                     }
                 };
                 if (it.nsteps == 0) {
                     // expert without tokens: an exact +0.0 tile, no accumulator involved
-                    uint32_t z[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) z[c] = 0u;
-                    for (int j = 0; j < nchunks; ++j) store_chunk(j, z);
+                    for (int j = 0; j < nchunks; ++j) store_chunk(j, [](int) { return 0u; });
                     continue;
                 }
                 // one lane waits, the warp follows its verdict (the TMEM loads below
@@ -1140,23 +1134,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                         else mbar_arrive_cluster(tempty_leader + 8 * buf);
                     }
                 };
-                // batches of at most four chunks, the short one first: the
-                // accumulator is released after the last batch's loads, so only
-                // the first batch's stores precede the release
-                const int first = nchunks - 4 * ((nchunks - 1) >> 2);
+                if (PACKED) {
+                    // five or six chunks: each is narrowed to bf16 pairs as soon
+                    // as it is loaded, so the whole row fits in registers and the
+                    // accumulator is released before any store
+                    uint32_t w[PACK_CHUNKS][16];
+#pragma unroll
+                    for (int j = 0; j < PACK_CHUNKS; ++j) {
+                        if (j < nchunks) {
+                            uint32_t v[32];
+                            tmem_ld_32x32b_x32(taddr + 32 * j, v);
+                            tmem_wait_ld();
+                            reg_fence(v);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[j][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                        }
+                    }
+                    release();
+#pragma unroll
+                    for (int j = 0; j < PACK_CHUNKS; ++j)
+                        if (j < nchunks) store_chunk(j, [&](int i) { return w[j][i]; });
+                } else {
+                    // batches of at most four chunks, the short one first: the
+                    // accumulator is released after the last batch's loads, so
+                    // only the first batch's stores precede the release
+                    const int first = nchunks - 4 * ((nchunks - 1) >> 2);
 #pragma unroll 1
-                for (int j0 = 0, nb = first; j0 < nchunks; j0 += nb, nb = 4) {
-                    uint32_t v[4][32];
+                    for (int j0 = 0, nb = first; j0 < nchunks; j0 += nb, nb = 4) {
+                        uint32_t v[4][32];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (j < nb) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
-                    tmem_wait_ld();
+                        for (int j = 0; j < 4; ++j)
+                            if (j < nb) tmem_ld_32x32b_x32(taddr + 32 * (j0 + j), v[j]);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-                    if (j0 + nb >= nchunks) release();
+                        for (int j = 0; j < 4; ++j) reg_fence(v[j]);
+                        if (j0 + nb >= nchunks) release();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (j < nb) store_chunk(j0 + j, v[j]);
+                        for (int j = 0; j < 4; ++j) {
+                            if (j < nb)
+                                store_chunk(j0 + j, [&](int i) { return pack_bf16x2(v[j][2 * i], v[j][2 * i + 1]); });
+                        }
+                    }
                 }
                 ++ntile;
             }
@@ -1170,15 +1188,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         using I2 = std::integral_constant<int, 2>;
         using I0 = std::integral_constant<int, 0>;
         using I3 = std::integral_constant<int, 3>;
-        switch ((p.acc_bufs == 2 ? 4 : 0) + (p.kn ? 2 : (p.tma_store ? 3 : (p.wide_stores ? 1 : 0)))) {
-            case 0: epilogue_loop(I1{}, I0{}); break;
-            case 1: epilogue_loop(I1{}, I1{}); break;
-            case 2: epilogue_loop(I1{}, I2{}); break;
-            case 3: epilogue_loop(I1{}, I3{}); break;
-            case 4: epilogue_loop(I2{}, I0{}); break;
-            case 5: epilogue_loop(I2{}, I1{}); break;
-            case 6: epilogue_loop(I2{}, I2{}); break;
-            default: epilogue_loop(I2{}, I3{}); break;
+        const int mode = p.kn ? 2 : (p.tma_store ? 3 : (p.wide_stores ? 1 : 0));
+        // (two accumulators only where tn <= 224: at most four chunks per warp)
+        const bool packed = p.acc_bufs == 1 && nchunks > 4 && nchunks <= 6 && mode != 0;
+        switch ((p.acc_bufs == 2 ? 4 : 0) + mode + (packed ? 8 : 0)) {
+            case 0: epilogue_loop(I1{}, I0{}, I0{}); break;
+            case 1: epilogue_loop(I1{}, I1{}, I0{}); break;
+            case 2: epilogue_loop(I1{}, I2{}, I0{}); break;
+            case 3: epilogue_loop(I1{}, I3{}, I0{}); break;
+            case 4: epilogue_loop(I2{}, I0{}, I0{}); break;
+            case 5: epilogue_loop(I2{}, I1{}, I0{}); break;
+            case 6: epilogue_loop(I2{}, I2{}, I0{}); break;
+            case 9: epilogue_loop(I1{}, I1{}, I1{}); break;
+            case 10: epilogue_loop(I1{}, I2{}, I1{}); break;
+            case 11: epilogue_loop(I1{}, I3{}, I1{}); break;
+            default: epilogue_loop(I2{}, I3{}, I0{}); break;
         }
     }
 
