@@ -970,7 +970,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         // the buffer index out of the registers the TMEM loads need
         auto epilogue_loop = [&](auto nbuf_tag, auto mode_tag, auto packed_tag) {
             constexpr uint32_t BUF_SHIFT = decltype(nbuf_tag)::value == 2 ? 1u : 0u;
-            // the whole drained row held as bf16 pairs (five or six chunks)
+            // the drained row held as bf16 pairs (five to seven chunks; a
+            // seventh is stored before the others are loaded)
             constexpr bool PACKED = decltype(packed_tag)::value != 0;
             constexpr int PACK_CHUNKS = 6;
             // 0: rows of A on the 256 side, 16-byte stores; 1: the same with
@@ -1135,13 +1136,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
                     }
                 };
                 if (PACKED) {
-                    // five or six chunks: each is narrowed to bf16 pairs as soon
-                    // as it is loaded, so the whole row fits in registers and the
-                    // accumulator is released before any store
+                    // five to seven chunks: a seventh is loaded and stored first;
+                    // chunks 0-5 are narrowed to bf16 pairs as soon as each is
+                    // loaded, so they fit in registers together and the
+                    // accumulator is released before they are stored
+                    if (nchunks > PACK_CHUNKS) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr + 32 * PACK_CHUNKS, v);
+                        tmem_wait_ld();
+                        reg_fence(v);
+                        store_chunk(PACK_CHUNKS, [&](int i) { return pack_bf16x2(v[2 * i], v[2 * i + 1]); });
+                    }
                     uint32_t w[PACK_CHUNKS][16];
 #pragma unroll
                     for (int j = 0; j < PACK_CHUNKS; ++j) {
-                        if (j < nchunks) {
+                        if (j < nchunks) {  // (always, with a seventh chunk)
                             uint32_t v[32];
                             tmem_ld_32x32b_x32(taddr + 32 * j, v);
                             tmem_wait_ld();
@@ -1190,7 +1199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         using I3 = std::integral_constant<int, 3>;
         const int mode = p.kn ? 2 : (p.tma_store ? 3 : (p.wide_stores ? 1 : 0));
         // (two accumulators only where tn <= 224: at most four chunks per warp)
-        const bool packed = p.acc_bufs == 1 && nchunks > 4 && nchunks <= 6 && mode != 0;
+        const bool packed = p.acc_bufs == 1 && nchunks > 4 && mode != 0;
         switch ((p.acc_bufs == 2 ? 4 : 0) + mode + (packed ? 8 : 0)) {
             case 0: epilogue_loop(I1{}, I0{}, I0{}); break;
             case 1: epilogue_loop(I1{}, I1{}, I0{}); break;
