@@ -1563,13 +1563,16 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
 // accumulator every tile waits for the previous tile's TMEM drain, which
 // short tiles do not amortise; tn = 256 (one MMA per 32-element chunk, six
 // stages, staged stores) measured best on most shapes; widths of 16 mod 32
-// store in 16-byte pieces, part of which falls inside that wait.
+// store in 16-byte pieces, part of which falls inside that wait. The fixed
+// part of tn = 352 was refitted after the epilogue came to release the
+// accumulator before its stores (forward and data gradient of the 16B
+// layers against tn = 256, per-step part kept).
 double gemm_tile_cost(int tn, bool wide_ok, double steps) {
     static const double ab[][2] = {
         // tn = 128, 144, ..., 448
         {1.09, 0.318}, {1.37, 0.316}, {1.25, 0.321}, {1.28, 0.333}, {1.09, 0.341}, {2.30, 0.340},
         {1.82, 0.360}, {1.64, 0.370}, {1.88, 0.346}, {4.72, 0.474}, {3.28, 0.466}, {5.44, 0.471},
-        {2.91, 0.473}, {2.63, 0.520}, {2.84, 0.525}, {2.86, 0.546}, {3.36, 0.529}, {5.27, 0.565},
+        {2.91, 0.473}, {2.63, 0.520}, {1.64, 0.525}, {2.86, 0.546}, {3.36, 0.529}, {5.27, 0.565},
         {3.00, 0.584}, {2.80, 0.598}, {2.25, 0.624}};
     if (tn < 128) {
         // narrower than measured: the long-tile column cost, scaled from tn = 128
