@@ -260,9 +260,11 @@ def tiling_reset():
 
 
 # (orientation mode, forced tile rows): the model's choice per orientation,
-# one-MMA tiles, two-MMA tiles (the second 16 columns wide, or 192), narrow tiles
+# one-MMA tiles, two-MMA tiles (the second 16 columns wide, or 192), narrow
+# tiles; the drain that holds a warp's row as bf16 pairs with five (272, 288,
+# 320), six (352) and seven (416, 448) chunks, whole and partial last ones
 TILINGS = [(1, 0), (2, 0), (1, 256), (2, 448), (1, 272), (2, 160), (1, 48), (1, 320), (1, 352), (1, 448),
-           (2, 352)]
+           (2, 352), (1, 416), (2, 416), (2, 288)]
 # epilogue stores: TMA stores through shared memory where their staging fits
 # (tn = 48, 256, 320, 352 with its half-chunk stored directly, 448; both
 # orientations), direct stores
