@@ -956,11 +956,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
         // ------------------------------------------------ epilogue (8 warps per CTA)
         // TMEM lane = M-side row of this CTA's half, column = N-side row of the
         // tile. Two warps share each 32-lane quarter, each draining half of the
-        // tn columns (at most 224) in 32-column loads: up to four chunks in
-        // flight at once; with more than four, the remainder (one to three
-        // chunks) is loaded and stored before the last four are loaded
-        // (registers hold 128 columns at most). The accumulator is released
-        // after the last load.
+        // tn columns (at most 224) in 32-column chunks. Up to four chunks are
+        // loaded together, the accumulator is released, then they are stored.
+        // Five to seven chunks (32-byte or TMA stores): a seventh is loaded and
+        // stored first, then chunks 0-5 are narrowed to bf16 pairs as each
+        // lands (96 registers), the accumulator is released and they are
+        // stored. With 16-byte stores, batches of at most four chunks (fp32
+        // registers hold 128 columns at most), the short one first, the
+        // release after the last batch's loads.
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int h = (warp - EPI_WARP0) >> 2;  // column half of the tile
         const int ncols = p.tn >> 1;
@@ -974,10 +977,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             // seventh is stored before the others are loaded)
             constexpr bool PACKED = decltype(packed_tag)::value != 0;
             constexpr int PACK_CHUNKS = 6;
-            // 0: rows of A on the 256 side, 16-byte stores; 1: the same with
-            // 32-byte stores; 2: rows of B on the 256 side (transposed: 4-byte
-            // stores, or TMA stores through shared memory when p.tma_store);
-            // 3: rows of A on the 256 side through shared memory and TMA stores
+            // 0: the M side on the output's rows (rows of A, or of X in the
+            // grouped GEMM), 16-byte stores; 1: the same with 32-byte stores;
+            // 2: the M side on the output's columns (rows of B; transposed:
+            // 4-byte stores, or TMA stores through shared memory when
+            // p.tma_store); 3: as 0, through shared memory and TMA stores
             constexpr int MODE = decltype(mode_tag)::value;
             uint32_t ntile = 0;  // non-empty tiles drained so far
             // MODE 3: this warp's staging buffers (2 KB each) and the next one to fill
