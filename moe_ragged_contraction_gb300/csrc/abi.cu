@@ -81,7 +81,7 @@ int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 // Token-contiguous E4M3 operand [rows][M] -> box of box_rows rows x 128 tokens,
 // 128-byte swizzle; out-of-range rows and tokens read as zero.
 int make_operand_map(CUtensorMap* map, const uint8_t* base, int rows, int64_t M, int box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     int rc = get_encoder(&enc);
     if (rc) return rc;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(rows)};
@@ -99,7 +99,7 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int rows, int64_t M,
 // box_rows rows x 128 elements x 1, 128-byte swizzle; out-of-range rows and
 // columns read as zero (rows past `rows` never reach the next depth slice).
 int make_operand_map3(CUtensorMap* map, const uint8_t* base, int64_t row_len, int rows, int depth, int box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     int rc = get_encoder(&enc);
     if (rc) return rc;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_len), static_cast<cuuint64_t>(rows),
@@ -120,7 +120,7 @@ int make_operand_map3(CUtensorMap* map, const uint8_t* base, int64_t row_len, in
 // (rows of cols bf16 not a multiple of 16 bytes, or out not 16-byte aligned).
 int make_out_map(CUtensorMap* map, uint16_t* out, int64_t cols, int64_t rows, int64_t depth) {
     if ((cols % 8) != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0) return 0;
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     if (get_encoder(&enc)) return 0;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(depth)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(cols) * rows * 2};
@@ -134,7 +134,7 @@ int make_out_map(CUtensorMap* map, uint16_t* out, int64_t cols, int64_t rows, in
 // Scale-factor workspace viewed as u32 [blocks][128] (one 512-byte block per
 // row); boxes of box_blocks whole blocks, no swizzle.
 int make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t blocks, int box_blocks) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     int rc = get_encoder(&enc);
     if (rc) return rc;
     cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(blocks)};
