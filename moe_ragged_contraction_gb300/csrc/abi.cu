@@ -295,13 +295,13 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
         // fewer issued instructions, less power, higher clocks under the power
         // cap. MXFP8_SUSPEND_NS overrides the hint (0 = plain polling). Set
         // once per device.
-        static bool hint_set[64] = {};
-        if (!hint_set[dev]) {
+        static std::atomic<bool> hint_set[64];
+        if (!hint_set[dev].load(std::memory_order_relaxed)) {
             const char* env = getenv("MXFP8_SUSPEND_NS");
             const long long ns = env ? atoll(env) : 50000;
             cudaError_t e = mxw::set_suspend_hint(static_cast<uint32_t>(ns < 0 ? 0 : (ns > 1000000 ? 1000000 : ns)));
             if (e != cudaSuccess) return fail_cuda(e, "suspend hint");
-            hint_set[dev] = true;
+            hint_set[dev].store(true, std::memory_order_relaxed);
         }
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);

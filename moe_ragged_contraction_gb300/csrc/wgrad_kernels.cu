@@ -36,6 +36,7 @@
 // partial step; the last step of a group issues only the ceil(rem/32) MMAs
 // that cover its tokens, so bytes past the group end (the next expert's, or
 // padding that may hold NaN) are loaded but never consumed.
+#include <atomic>
 #include <type_traits>
 
 #include "mxw_internal.h"
@@ -1439,12 +1440,14 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
                           sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
         // (large E can need more than the 48 KB default of shared memory)
-        static bool prep_attr[64] = {};
+        // (per-device caches below: idempotent, so concurrent first calls may
+        // both set them; atomics keep that free of data races)
+        static std::atomic<bool> prep_attr[64];
         if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
-        if (!prep_attr[a.dev]) {
+        if (!prep_attr[a.dev].load(std::memory_order_relaxed)) {
             cudaError_t e0 = cudaFuncSetAttribute(wgrad_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
             if (e0 != cudaSuccess) return e0;
-            prep_attr[a.dev] = true;
+            prep_attr[a.dev].store(true, std::memory_order_relaxed);
         }
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wgrad_prep, PREP_THREADS, sm);
@@ -1490,9 +1493,10 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     // per device: the shared-memory opt-in and the number of CTA pairs that
     // can be resident at once (the persistent grid; one CTA per SM whatever
     // the tile, as the register file holds only one)
-    static int max_pairs[64] = {};
+    static std::atomic<int> max_pairs[64];
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (max_pairs[dev] == 0) {
+    int mp_dev = max_pairs[dev].load(std::memory_order_relaxed);
+    if (mp_dev == 0) {
         cudaError_t e = cudaFuncSetAttribute(wgrad_main, cudaFuncAttributeMaxDynamicSharedMemorySize, MAIN_SMEM_MAX);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t q = {};
@@ -1503,7 +1507,8 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
         e = cudaOccupancyMaxActiveClusters(&clusters, wgrad_main, &q);
         if (e != cudaSuccess) return e;
         if (clusters < 1) return cudaErrorInvalidConfiguration;
-        max_pairs[dev] = clusters;
+        max_pairs[dev].store(clusters, std::memory_order_relaxed);
+        mp_dev = clusters;
     }
     mp.tiles_n = tc.tiles_n;
     mp.tn = tc.tn;
@@ -1524,7 +1529,7 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     // the caller asks for TMA stores (output map built); they run where staging fits
     mp.tma_store = (mp.tma_store && geo.stg_bufs > 0 && (!tc.kn || mp.mode == 0)) ? 1 : 0;
     mp.b_stage = geo.b_stage;
-    const int pairs = static_cast<int>(items < max_pairs[dev] ? (items > 0 ? items : 1) : max_pairs[dev]);
+    const int pairs = static_cast<int>(items < mp_dev ? (items > 0 ? items : 1) : mp_dev);
     if (ev_before) {
         cudaError_t e = cudaEventRecord(ev_before, stream);
         if (e != cudaSuccess) return e;
@@ -1660,12 +1665,12 @@ cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap* maps, const char**
         pa.M = a.M;
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
                           sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
-        static bool attr_set[64] = {};
+        static std::atomic<bool> attr_set[64];
         if (a.dev < 0 || a.dev >= 64) return cudaErrorInvalidDevice;
-        if (!attr_set[a.dev]) {
+        if (!attr_set[a.dev].load(std::memory_order_relaxed)) {
             cudaError_t e0 = cudaFuncSetAttribute(gemm_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
             if (e0 != cudaSuccess) return e0;
-            attr_set[a.dev] = true;
+            attr_set[a.dev].store(true, std::memory_order_relaxed);
         }
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_prep, PREP_THREADS, sm);
