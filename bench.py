@@ -13,6 +13,15 @@ Metric: TFLOP/s = 2 N K sum_g len_g / time. Prints one JSON line.
 
 --impl reference times the CPU oracle (the plain fp64 definition) on the
 host's cores on a bounded sample of the same workload.
+
+Default workload: the 671B down-projection expert shape (E=32, N=7168,
+K=2048, M=524288 tokens), the largest of the named workloads in tokens and
+bytes that runs on one GPU; the others run with --config.
+
+Besides the mean over the K timed steps (the reported value), the line
+carries the spread of those steps and of three passes of at least one second
+of back-to-back calls (no L2 flush, no synchronisation between calls), as
+median, minimum and maximum.
 """
 from __future__ import annotations
 
@@ -31,7 +40,7 @@ import numpy as np  # noqa: E402
 
 from moe_ragged_contraction_gb300 import inputs as I  # noqa: E402
 
-DEFAULT_CONFIG = "16B"
+DEFAULT_CONFIG = "671Bd"
 METRIC = "TFLOP/s (2*N*K*sum(M_g)) ragged MXFP8 wgrad, % of GB300 MXFP8 tensor peak"
 FP8_OVER_BF16 = 2.0  # nominal dense ratio: 4.5 PF fp8 / 2.25 PF bf16
 L2_FLUSH_BYTES = 256 << 20
@@ -197,38 +206,76 @@ def make_device_inputs(name: str, device):
     return ops[0], ops[1], ops[2], ops[3], offs
 
 
-def cpu_oracle_rate(A, sA, B, sB, offs, w, target_s: float, threads: int, seed: int = 0):
-    """Time the oracle on a bounded sample: whole output rows (all K columns)
-    of every non-empty expert, as many rows as fit ~target_s seconds.
+# ------------------------------------------------------------------ CPU oracle sample (baseline)
+
+POOL_BLOCKS = 8      # 16-row blocks of A and of B whose rows the oracle sample draws from
+POOL_BLOCK_ROWS = 16
+
+
+def pool_rows(w, seed: int = 0):
+    """Rows of A (output rows n) and of B (output columns k) that the CPU
+    sample draws its output elements from: POOL_BLOCKS random 16-row blocks of
+    each (whole blocks, so that the host-side generator, seeded per 16-row
+    block, can produce exactly these rows)."""
+    rng = np.random.default_rng(7000 + seed)
+
+    def pick(rows):
+        nblk = (rows + POOL_BLOCK_ROWS - 1) // POOL_BLOCK_ROWS
+        blks = np.sort(rng.choice(nblk, size=min(POOL_BLOCKS, nblk), replace=False))
+        r = (blks[:, None] * POOL_BLOCK_ROWS + np.arange(POOL_BLOCK_ROWS)[None, :]).ravel()
+        return r[r < rows]
+
+    return pick(w.N), pick(w.K)
+
+
+def oracle_sample_rate(Ap, sAp, Bp, sBp, offs, w, target_s: float, threads: int, seed: int = 0):
+    """Time the oracle on a bounded sample of the workload's output: for every
+    non-empty expert, a number of output rows n drawn at random from the
+    pooled rows Ap = A[pool_n], each with every pooled column k of
+    Bp = B[pool_k], in the order the oracle walks the full output (expert,
+    then row, then column); as many rows as fit about target_s seconds.
     Returns (TFLOP/s, seconds, description)."""
     import oracle
 
+    offs = np.asarray(offs)
     sizes = np.diff(np.concatenate([[0], offs]))
     live = np.nonzero(sizes > 0)[0]
     rng = np.random.default_rng(seed)
-
-    def sample(rows_per_expert):
-        gs, ns, ks = [], [], []
-        for g in live:
-            for n in rng.integers(0, w.N, rows_per_expert):
-                gs.append(np.full(w.K, g)); ns.append(np.full(w.K, n)); ks.append(np.arange(w.K))
-        return (np.concatenate(gs).astype(np.int32), np.concatenate(ns).astype(np.int32),
-                np.concatenate(ks).astype(np.int32))
+    pn, pk = Ap.shape[0], Bp.shape[0]
 
     def run(rows):
-        g, n, k = sample(rows)
+        gs, ns = [], []
+        for g in live:
+            for n in np.sort(rng.integers(0, pn, rows)):
+                gs.append(np.full(pk, g)); ns.append(np.full(pk, n))
+        g = np.concatenate(gs).astype(np.int32)
+        n = np.concatenate(ns).astype(np.int32)
+        k = np.tile(np.arange(pk, dtype=np.int32), rows * len(live))
         flop = 2.0 * float(np.sum(sizes[g]))
         t0 = time.perf_counter()
-        oracle.wgrad_points(A, sA, B, sB, offs, w.E, w.N, w.K, w.M, g, n, k, nthreads=threads)
+        oracle.wgrad_points(Ap, sAp, Bp, sBp, offs, w.E, pn, pk, w.M, g, n, k, nthreads=threads)
         return flop, time.perf_counter() - t0
 
-    flop, dt = run(1)  # calibration
-    rows = int(max(1, min(w.N, round(target_s / max(dt, 1e-6)))))
-    if rows > 1:
-        flop, dt = run(rows)
-    desc = (f"{rows} random full output row(s) (all {w.K} columns) of each of the {len(live)} non-empty experts, "
-            f"{flop / 2:.3g} MACs")
+    rows = 2
+    flop, dt = run(rows)  # calibration
+    rows = int(max(1, round(rows * target_s / max(dt, 1e-6))))
+    flop, dt = run(rows)
+    desc = (f"{rows} output rows x {pk} columns of each of the {len(live)} non-empty experts "
+            f"(rows drawn from {pn} rows of A, columns the {pk} rows of B of {POOL_BLOCKS} random "
+            f"16-row blocks of each), {flop / 2:.3g} MACs, rate extrapolated to the whole workload")
     return flop / dt / 1e12, dt, desc
+
+
+def bench_config(name: str, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    w = I.WORKLOADS[name]
+    return {"workload": name, "E": w.E, "N": w.N, "K": w.K, "M": w.M, "routing": w.description,
+            "l2": L2Flush.DESCRIPTION, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def spread(values) -> dict:
+    v = np.asarray(values, dtype=np.float64)
+    return {"median": float(np.median(v)), "min": float(v.min()), "max": float(v.max()), "n": int(v.size)}
 
 
 def hold_gpu(steps: int) -> None:
@@ -281,7 +328,7 @@ def bench_gpu(args):
         flush()
         step()
     torch.cuda.synchronize()
-    t_end = time.perf_counter() + 0.5
+    t_end = time.perf_counter() + (0.0 if args.quick else 0.5)
     while time.perf_counter() < t_end:
         for _ in range(20):
             step()
@@ -321,56 +368,75 @@ def bench_gpu(args):
         step(main_pair=evm[i])
     torch.cuda.synchronize()
     main_ms = [a.elapsed_time(b) for a, b in evm]
+    # spread: three passes of at least one second of back-to-back calls each
+    # (no L2 flush, no synchronisation between calls), bracketed by events
+    calls = int(max(10, np.ceil(1.0 / max(1e-6, float(np.mean(step_ms)) * 1e-3))))
+    b2b = []
+    for _ in range(0 if args.quick else 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_gpu(min(calls, 200))
+        e0.record(stream)
+        for _ in range(calls):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        b2b.append(float(w.flop) / (e0.elapsed_time(e1) / calls * 1e-3) / 1e12)
     assert mx.device_status(clear=True) == 0, "device flagged an error during the benchmark"
 
-    # end to end through the public API with host buffers: every step copies its
-    # inputs host -> device (pinned host memory) and its result device -> host
-    # inside the timed interval. Consecutive steps overlap like a streaming
-    # pipeline: the copy-in of step i+1, the call of step i and the copy-out of
-    # step i-1 run on three streams over two device buffer sets, ordered by
-    # events (a set's inputs are overwritten only after its call finished, its
-    # output only after it was copied out).
-    hA, hsA, hB, hsB, hoffs = (t.cpu().pin_memory() for t in (A, sA, B, sB, offs))
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB, hoffs))
-    d2h = hout.numel() * hout.element_size()
-    sets = [tuple(torch.empty_like(t) for t in (A, sA, B, sB, offs, out)) for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    ev_in = [torch.cuda.Event() for _ in range(2)]    # the set's inputs have landed
-    ev_used = [torch.cuda.Event() for _ in range(2)]  # the set's call has finished
-    ev_out = [torch.cuda.Event() for _ in range(2)]   # the set's output has been copied out
+    e2e = None
+    if not args.quick and not args.no_e2e:
+        # end to end through the public API with host buffers: every step copies its
+        # inputs host -> device (pinned host memory) and its result device -> host
+        # inside the timed interval. Consecutive steps overlap like a streaming
+        # pipeline: the copy-in of step i+1, the call of step i and the copy-out of
+        # step i-1 run on three streams over two device buffer sets, ordered by
+        # events (a set's inputs are overwritten only after its call finished, its
+        # output only after it was copied out).
+        hA, hsA, hB, hsB, hoffs = (t.cpu().pin_memory() for t in (A, sA, B, sB, offs))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB, hoffs))
+        d2h = hout.numel() * hout.element_size()
+        sets = [tuple(torch.empty_like(t) for t in (A, sA, B, sB, offs, out)) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        ev_in = [torch.cuda.Event() for _ in range(2)]    # the set's inputs have landed
+        ev_used = [torch.cuda.Event() for _ in range(2)]  # the set's call has finished
+        ev_out = [torch.cuda.Event() for _ in range(2)]   # the set's output has been copied out
 
-    def e2e_step(i):
-        b = i % 2
-        dA, dsA, dB, dsB, doffs, dout = sets[b]
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_used[b])
-            for d, h in ((dA, hA), (dsA, hsA), (dB, hB), (dsB, hsB), (doffs, hoffs)):
-                d.copy_(h, non_blocking=True)
-            ev_in[b].record(s_in)
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_out[b])
-        mx.wgrad_grouped(dA, dsA, dB, dsB, doffs, out=dout, stream=stream)
-        ev_used[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_used[b])
-            hout.copy_(dout, non_blocking=True)
-            ev_out[b].record(s_out)
+        def e2e_step(i):
+            b = i % 2
+            dA, dsA, dB, dsB, doffs, dout = sets[b]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_used[b])
+                for d, h in ((dA, hA), (dsA, hsA), (dB, hB), (dsB, hsB), (doffs, hoffs)):
+                    d.copy_(h, non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])
+            mx.wgrad_grouped(dA, dsA, dB, dsB, doffs, out=dout, stream=stream)
+            ev_used[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_used[b])
+                hout.copy_(dout, non_blocking=True)
+                ev_out[b].record(s_out)
 
-    for i in range(max(3, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    s_in.wait_stream(stream)
-    s_out.wait_stream(stream)
-    for i in range(K):
-        e2e_step(i)
-    stream.wait_stream(s_in)
-    stream.wait_stream(s_out)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
+        for i in range(max(3, args.warmup)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(K):
+            e2e_step(i)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / K
+        e2e = {"value": float(w.flop) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "pipelining": "copy-in, call and copy-out of consecutive steps overlap (three streams, "
+                             "two device buffer sets)"}
     clocks = sampler.stop()
 
     flop = float(w.flop)
@@ -399,10 +465,13 @@ def bench_gpu(args):
     result = None
     if rank == 0:
         cpu = None
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and not args.quick and world == 1:
             threads = len(os.sched_getaffinity(0))
-            rate, secs, desc = cpu_oracle_rate(A.cpu().numpy(), sA.cpu().numpy(), B.cpu().numpy(),
-                                               sB.cpu().numpy(), offs.cpu().numpy(), w, args.cpu_seconds, threads)
+            rn, rk = pool_rows(w)
+            rn_t, rk_t = torch.from_numpy(rn).to(device), torch.from_numpy(rk).to(device)
+            Ap, sAp, Bp, sBp = (t.index_select(0, r).cpu().numpy()
+                                for t, r in ((A, rn_t), (sA, rn_t), (B, rk_t), (sB, rk_t)))
+            rate, secs, desc = oracle_sample_rate(Ap, sAp, Bp, sBp, offs.cpu().numpy(), w, args.cpu_seconds, threads)
             cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": f"{desc}; {secs:.1f} s on the host (fp64 plain loops)"}
         result = {
@@ -418,16 +487,16 @@ def bench_gpu(args):
             "vs_baseline": None,
             "dtype": "mxfp8_e4m3 (e8m0 block-32 scales), fp32 accumulate, bf16 out",
             "data": "synthetic (seeded routing and N(0,1)/Student-t operands, quantised on the GPU)",
-            "config": {"workload": args.config, "E": w.E, "N": w.N, "K": w.K, "M": w.M,
-                       "routing": w.description, "l2": L2Flush.DESCRIPTION,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": bench_config(args.config, world),
             "pct_of_mxfp8_peak": 100.0 * value / world / peak,
+            "spread": {"unit": "TFLOP/s",
+                       "timed_steps": spread([flop / (t * 1e-3) / 1e12 for t in step_ms]),
+                       "back_to_back": dict(spread(b2b), calls_per_pass=calls,
+                                            how="3 passes of >= 1 s of back-to-back calls, no L2 flush")
+                       if b2b else None},
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "pipelining": "copy-in, call and copy-out of consecutive steps overlap (three streams, "
-                                  "two device buffer sets)"},
+            "e2e": e2e,
             "gpu_launches": 2 * K,
             "clocks": clocks,
         }
@@ -693,36 +762,41 @@ def bench_gemm(args):
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 
-def _host_inputs(name: str):
-    """Host operands for the reference arm: seeded fp32 quantised by the
-    oracle's CPU quantiser (no GPU involved)."""
+def _host_pool(name: str):
+    """Host operands for the reference arm, only the pooled rows the oracle
+    sample draws from (pool_rows): seeded fp32 rows quantised by the oracle's
+    CPU quantiser (no GPU involved)."""
     import oracle
 
     w = I.WORKLOADS[name]
-    ops = []
-    for stream, rows in ((0, w.N), (1, w.K)):
-        q = np.empty((rows, w.M), np.uint8)
-        s = np.empty((rows, w.M // 32), np.uint8)
-        for r0 in range(0, rows, 256):
-            r1 = min(rows, r0 + 256)
-            q[r0:r1], s[r0:r1] = oracle.quantize_tokenwise(I.host_operand(r1 - r0, w.M, w.seed, stream, w.dist, row0=r0))
-        ops += [q, s]
-    return ops[0], ops[1], ops[2], ops[3], I.offsets(I.group_sizes(name))
+    rn, rk = pool_rows(w)
+    out = []
+    for stream, rows in ((0, rn), (1, rk)):
+        q = np.empty((rows.size, w.M), np.uint8)
+        s = np.empty((rows.size, w.M // 32), np.uint8)
+        for i in range(0, rows.size, POOL_BLOCK_ROWS):
+            r0 = int(rows[i])
+            nr = min(POOL_BLOCK_ROWS, rows.size - i)
+            x = I.host_operand(nr, w.M, w.seed, stream, w.dist, row0=r0)
+            q[i:i + nr], s[i:i + nr] = oracle.quantize_tokenwise(x)
+        out += [q, s]
+    return out[0], out[1], out[2], out[3], I.offsets(I.group_sizes(name))
 
 
 def bench_reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     w = I.WORKLOADS[args.config]
-    A, sA, B, sB, offs = _host_inputs(args.config)
+    Ap, sAp, Bp, sBp, offs = _host_pool(args.config)
     threads = len(os.sched_getaffinity(0))
     per_step = max(0.5, args.ref_step_seconds)
     for i in range(args.warmup):
-        cpu_oracle_rate(A, sA, B, sB, offs, w, per_step / 4, threads, seed=i)
+        oracle_sample_rate(Ap, sAp, Bp, sBp, offs, w, per_step / 4, threads, seed=i)
     rates, secs, desc = [], 0.0, ""
     for i in range(args.steps):
-        r, dt, desc = cpu_oracle_rate(A, sA, B, sB, offs, w, per_step, threads, seed=1000 + i)
+        r, dt, desc = oracle_sample_rate(Ap, sAp, Bp, sBp, offs, w, per_step, threads, seed=1000 + i)
         rates.append(r)
         secs += dt
     value = float(np.mean(rates))
@@ -731,7 +805,7 @@ def bench_reference_arm(args):
         "metric": METRIC,
         "value": value,
         "unit": "TFLOP/s",
-        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / max(1, args.steps),
@@ -740,7 +814,8 @@ def bench_reference_arm(args):
         "vs_baseline": None,
         "dtype": "f64 (exact E4M3/E8M0 decode, fp64 accumulate, bf16 out)",
         "data": "synthetic (seeded routing and N(0,1)/Student-t operands, quantised on the host)",
-        "config": {"workload": args.config, "E": w.E, "N": w.N, "K": w.K, "M": w.M, "routing": w.description},
+        "config": bench_config(args.config, world),
+        "spread": {"unit": "TFLOP/s", "timed_steps": spread(rates)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"each step: {desc}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -762,11 +837,25 @@ def main():
                     help="print a context line with vendor BF16 grouped / dense MXFP8 GEMM timings instead")
     ap.add_argument("--quantizer", action="store_true",
                     help="print a line for the fused bf16 quantise-and-transpose of the workload's operands instead")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload's expert shapes and routing recipe with this many tokens instead "
+                         "(profiler captures on a small case)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="run the workload's expert shapes with this many experts, each with the workload's mean "
+                         "token run (balanced routing; profiler captures on a small case)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only: no settle loop, spread passes, end-to-end leg or CPU "
+                         "baseline (profiler runs)")
     ap.add_argument("--gemm", action="store_true",
                     help="print a line for the layer's forward and data-gradient grouped GEMMs (ragged rows) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.tokens:
+        args.config = I.with_tokens(args.config, args.tokens)
+    if args.experts:
+        args.config = I.with_experts(args.config, args.experts)
     if args.comparators:
         res = bench_comparators(args)
     elif args.quantizer:

@@ -169,6 +169,41 @@ _RECIPES = {
 }
 
 
+def with_tokens(name: str, M: int) -> str:
+    """Registers (once) and returns the name of a copy of workload `name` with
+    M tokens instead of its own, routed by the same recipe: the same expert
+    shapes and routing pattern at a smaller size (profiler captures)."""
+    from dataclasses import replace
+
+    if M % 32 or M < 32 * WORKLOADS[name].E:
+        raise ValueError(f"M={M} must be a multiple of 32 and give every expert at least 32 tokens")
+    new = f"{name}@M{M}"
+    if new not in WORKLOADS:
+        w = WORKLOADS[name]
+        WORKLOADS[new] = replace(w, name=new, M=M, description=f"{w.description}; scaled to M={M} tokens")
+        _RECIPES[new] = _RECIPES[name]
+    return new
+
+
+def with_experts(name: str, E: int) -> str:
+    """Registers (once) and returns the name of a copy of workload `name` with
+    E experts and the same mean tokens per expert, routed evenly (every
+    expert gets the mean run, in 32-token units): the expert shapes and run
+    lengths of the workload at a fraction of its size (profiler captures)."""
+    from dataclasses import replace
+
+    w = WORKLOADS[name]
+    if E < 1:
+        raise ValueError("E must be >= 1")
+    M = max(32, int(round(w.M / w.E / 32.0)) * 32) * E
+    new = f"{name}@E{E}"
+    if new not in WORKLOADS:
+        WORKLOADS[new] = replace(w, name=new, E=E, M=M,
+                                 description=f"{w.description}; {E} experts with its mean run of {M // E} tokens each")
+        _RECIPES[new] = _sizes_balanced
+    return new
+
+
 def group_sizes(name: str) -> np.ndarray:
     """Per-expert token counts (int64 [E]); multiples of 32 summing to M."""
     w = WORKLOADS[name]
