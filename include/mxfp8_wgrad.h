@@ -36,8 +36,9 @@
  *    enqueued. Errors the device detects (invalid offsets, a pipeline wait
  *    that ran out) set bits of a device status word read by
  *    mxfp8_device_status().
- *  - Requires an sm_103 (GB300) or sm_100-family device with the library
- *    built for it.
+ *  - Requires an sm_103 (GB300) device: the library is built for sm_103a
+ *    only, and every entry point that touches the device returns
+ *    MXFP8_EUNSUPPORTED on any other.
  */
 #ifndef MXFP8_WGRAD_H
 #define MXFP8_WGRAD_H
@@ -54,7 +55,7 @@ extern "C" {
 #define MXFP8_EINVAL (-1)       /* null pointer, negative or zero size, M % 32 != 0, E too large */
 #define MXFP8_EALIGN (-2)       /* a pointer not 16-byte aligned, or K % 8 != 0 */
 #define MXFP8_ECUDA (-3)        /* a CUDA runtime/driver error (message attached) */
-#define MXFP8_EUNSUPPORTED (-4) /* the current device is not an sm_100-family GPU */
+#define MXFP8_EUNSUPPORTED (-4) /* the current device is not an sm_103 (GB300) GPU */
 #define MXFP8_ENOWS (-5)        /* caller workspace smaller than mxfp8_wgrad_workspace_bytes() */
 
 /* Bits of the device status word (mxfp8_device_status). */
@@ -213,13 +214,21 @@ int mxfp8_device_status(int32_t* status, int clear);
  * MXFP8_NOALLOC_SCRATCH_BYTES are rejected with MXFP8_ENOWS and a message,
  * before any work is enqueued (e.g. the 16B shapes fit; the 671B shapes do not).
  *
- * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture. Every call on a device shares the one
- * array, and the array keeps whatever the last call left in it (each call
- * rewrites all the scratch it reads, so nothing needs clearing): calls whose
- * work overlaps on the GPU (different streams, no ordering between them) race
- * on it and must be avoided by the caller.
+ * Set-up: the CUDA runtime loads device code lazily, so the array (and the
+ * kernels' code) is placed in device memory when first used in a CUDA
+ * context. This entry point's first call in each context does that set-up: it
+ * loads both and looks up the array's device address with that context
+ * current (cudaGetSymbolAddress). That first call is the one moment it
+ * commits device memory (the array's 32 MiB); every later call in the context
+ * allocates nothing. A call with E == 0 (and valid N, K, M; the pointers are
+ * not used) performs only the set-up: make it before reserving the rest of
+ * the device's memory, and before any stream capture.
+ *
+ * Every call in a context shares the one array, and the array keeps whatever
+ * the last call left in it (each call rewrites all the scratch it reads, so
+ * nothing needs clearing): calls whose work overlaps on the GPU (different
+ * streams, no ordering between them) race on it and must be avoided by the
+ * caller.
  */
 int mxfp8_wgrad_grouped_noalloc(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                                 const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,

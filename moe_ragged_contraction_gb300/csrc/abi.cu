@@ -43,7 +43,7 @@ std::mutex g_mu;
 DeviceInfo g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Device checks: an sm_100-family GPU with the library's sm_103a build.
+// Device checks: an sm_103 (GB300) GPU, the only target the library is built for.
 int current_device(int* dev, DeviceInfo* info) {
     cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");

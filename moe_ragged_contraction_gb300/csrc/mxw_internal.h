@@ -116,6 +116,10 @@ cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_
 cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s,
                                       cudaStream_t stream);
 
+// Loads the module holding the weight-gradient kernels on the current device
+// (the runtime otherwise loads it at the first launch), without launching.
+cudaError_t load_kernel_modules();
+
 // Sets the calling thread's mxfp8_last_error() message; returns `code`.
 int set_last_error(int code, const char* msg);
 

@@ -224,6 +224,34 @@ __device__ __forceinline__ void tc_mma_mxf8_pair_elect(uint32_t d_tmem, uint64_t
         : "memory");
 }
 
+// As tc_mma_mxf8_pair_elect, keeping this MMA's A tile in the tensor core's
+// collector buffer (`fill`) so that the next MMA, issued right after it by
+// the same thread with the same A tile, reads A from there (`lastuse`, which
+// then releases the buffer) instead of from shared memory again.
+__device__ __forceinline__ void tc_mma_mxf8_pair_elect_fill(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X.collector::a::fill [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_mxf8_pair_elect_lastuse(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                               uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X.collector::a::lastuse [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Each CTA of the pair copies 32 rows x 16 bytes from its own shared memory
 // at `sdesc` into its own TMEM at `taddr`, replicated to the four 32-lane
 // quarters.

@@ -43,6 +43,12 @@
 #include "mxw_ptx.cuh"
 #include "../../include/mxfp8_wgrad.h"
 
+// 1: tiles wider than 256 columns (two MMAs per 32-token chunk, one A tile)
+// read A from shared memory once per chunk through the collector buffer.
+#ifndef MXW_COLLECTOR_A
+#define MXW_COLLECTOR_A 0
+#endif
+
 namespace mxw {
 
 __device__ int g_device_status = 0;
@@ -770,10 +776,20 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
                     const uint32_t sel = (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
                     const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t ad = desc_kmajor_sw128(a_s + 32 * kk);
-                    tc_mma_mxf8_pair_elect(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t, acc);
-                    if (TWO)
-                        tc_mma_mxf8_pair_elect(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk), idesc2 | sel,
-                                               sfa_t, sfb_t + 8, acc);
+                    if (TWO && MXW_COLLECTOR_A) {
+                        // both MMAs of the chunk multiply the same A tile: the
+                        // second reads it from the collector buffer
+                        tc_mma_mxf8_pair_elect_fill(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t,
+                                                    sfb_t, acc);
+                        tc_mma_mxf8_pair_elect_lastuse(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk),
+                                                       idesc2 | sel, sfa_t, sfb_t + 8, acc);
+                    } else {
+                        tc_mma_mxf8_pair_elect(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t,
+                                               acc);
+                        if (TWO)
+                            tc_mma_mxf8_pair_elect(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk),
+                                                   idesc2 | sel, sfa_t, sfb_t + 8, acc);
+                    }
                 }
                 tc_commit_pair_elect(x.bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
             }
@@ -1408,6 +1424,13 @@ size_t ws_bytes_any_orientation(int E, int N, int K, int64_t M, int force_tn) {
         if (L.total > most) most = L.total;
     }
     return most;
+}
+
+cudaError_t load_kernel_modules() {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, wgrad_prep);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, wgrad_main);
+    return e;
 }
 
 cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char** what) {
