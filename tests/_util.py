@@ -47,10 +47,28 @@ def same_bits_signless_zero(a, b):
     return np.array_equal(a, b)
 
 
-def sample_indices(E, N, K, rng, rows=4, cols=4, rand=1024):
+def sample_indices(E, N, K, rng, rows=8, cols=8, rand=4096, tiling=None, corner_experts=8):
     """Per expert: `rows` full output rows (first, last, random), `cols` full
-    columns, and `rand` random elements. Returns int32 arrays (g, n, k)."""
+    columns (likewise) and `rand` random elements. Given the library's tiling
+    (a dict with kn, tn, tiles_m, tiles_n as mxfp8_wgrad_tile_config reports
+    it), also every element of the four corner tiles of the output (the first
+    and last tile of the first and last tile row: the last ones are clipped at
+    the output's edges) for `corner_experts` experts (the first, the last and
+    random others; all of them when E is at most that). Returns int32 arrays
+    (g, n, k)."""
     gs, ns, ks = [], [], []
+    corners = []
+    if tiling is not None:
+        # tile extents along n (output rows) and k (output columns)
+        tr, tc = (tiling["tn"], 256) if tiling["kn"] else (256, tiling["tn"])
+        rt = sorted({0, (N - 1) // tr})
+        ct = sorted({0, (K - 1) // tc})
+        for a in rt:
+            for b in ct:
+                nn = np.arange(a * tr, min(N, (a + 1) * tr))
+                kk = np.arange(b * tc, min(K, (b + 1) * tc))
+                corners.append((np.repeat(nn, kk.size), np.tile(kk, nn.size)))
+    cg = set(range(E)) if E <= corner_experts else {0, E - 1, *rng.choice(E, corner_experts - 2, replace=False).tolist()}
     for g in range(E):
         rsel = sorted({0, N - 1, *rng.integers(0, N, max(0, rows - 2)).tolist()})
         csel = sorted({0, K - 1, *rng.integers(0, K, max(0, cols - 2)).tolist()})
@@ -59,5 +77,7 @@ def sample_indices(E, N, K, rng, rows=4, cols=4, rand=1024):
         for k in csel:
             gs.append(np.full(N, g)); ns.append(np.arange(N)); ks.append(np.full(N, k))
         gs.append(np.full(rand, g)); ns.append(rng.integers(0, N, rand)); ks.append(rng.integers(0, K, rand))
+        for nn, kk in (corners if g in cg else []):
+            gs.append(np.full(nn.size, g)); ns.append(nn); ks.append(kk)
     cat = lambda v: np.concatenate(v).astype(np.int32)  # noqa: E731
     return cat(gs), cat(ns), cat(ks)

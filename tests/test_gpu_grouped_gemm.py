@@ -165,3 +165,48 @@ def test_grouped_gemm_edge_shapes(E, M, N, K, sizes):
     bad = tolerance_violations(outs[0], ref, aacc)
     assert not bad.any(), f"{bad.sum()} of {bad.size} out of tolerance"
     assert np.all(outs[0][int(offs[-1]):] == 0), "padding rows not +0"
+
+
+@pytest.mark.parametrize("name,product", [
+    ("671Bgu", "forward"), ("671Bgu", "dgrad"), ("671Bd", "forward"), ("671Bd", "dgrad"),
+])
+def test_grouped_gemm_671B_layer_shapes_sampled(name, product):
+    """The 671B expert layers' forward and data-gradient products at full
+    size, on the workload's routing, in the launch the grouped-GEMM benchmark
+    times: forward X [M, K] x W [E, N, K]^T, data gradient dY [M, N] x
+    W^T [E, K, N]^T. Sampled elements against the oracle (full rows at both
+    ends, at every group boundary and at random, plus 4,096 random elements),
+    the whole NaN-poisoned output finite, two runs identical."""
+    w = I.WORKLOADS[name]
+    E, M = w.E, w.M
+    rows_w, cols = (w.N, w.K) if product == "forward" else (w.K, w.N)  # W [E, rows_w, cols], contraction over cols
+    offs = I.offsets(I.group_sizes(name))
+    block = max(256, (1 << 24) // cols // 16 * 16)  # rows per host-generated block (a multiple of 16)
+    X, sX = quantised_operand(M, cols, seed=w.seed, stream=30 if product == "forward" else 31, dist=w.dist,
+                              block_rows=block)
+    W = np.empty((E, rows_w, cols), np.uint8)
+    sW = np.empty((E, rows_w, cols // 32), np.uint8)
+    for g in range(E):
+        W[g], sW[g] = quantised_operand(rows_w, cols, seed=w.seed, stream=40 + g, block_rows=block)
+    dX, dsX, dW, dsW, doffs = dev(X), dev(sX), dev(W), dev(sW), dev(offs)
+    mx.device_status(clear=True)
+    out = torch.empty((M, rows_w), dtype=torch.bfloat16, device="cuda")
+    out.view(torch.int16).fill_(-1)
+    mx.grouped_gemm(dX, dsX, dW, dsW, doffs, out=out)
+    out2 = torch.empty_like(out)
+    out2.view(torch.int16).fill_(-1)
+    mx.grouped_gemm(dX, dsX, dW, dsW, doffs, out=out2)
+    torch.cuda.synchronize()
+    assert mx.device_status(clear=True) == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)), "not bit-reproducible"
+    del out2
+    assert torch.isfinite(out.float()).all(), "unwritten (NaN-poisoned) or non-finite elements"
+    rng = np.random.default_rng(w.seed + (0 if product == "forward" else 1))
+    live = offs[:-1][(offs[:-1] > 0) & (offs[:-1] < M)]
+    rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 8), live - 1, live])).astype(np.int64)
+    t = np.concatenate([np.repeat(rows, rows_w), rng.integers(0, M, 4096)])
+    n = np.concatenate([np.tile(np.arange(rows_w), rows.size), rng.integers(0, rows_w, 4096)])
+    ref, _, aacc = oracle.grouped_gemm(X, sX, W, sW, offs, E, M, rows_w, cols, points=(t, n), want_acc=True)
+    got = out.view(torch.int16)[torch.from_numpy(t).cuda(), torch.from_numpy(n).cuda()].cpu().numpy().view(np.uint16)
+    bad = tolerance_violations(got, ref, aacc)
+    assert not bad.any(), f"{bad.sum()} of {bad.size} sampled elements out of tolerance"

@@ -1,6 +1,7 @@
 """Full-size parity on every named workload, in the launch configuration the
 benchmark times (the plain C-ABI call): sampled output elements against the
-oracle (full rows and columns of every expert plus random elements), the
+oracle (8 full rows, 8 full columns, the four corner tiles of the
+library's tiling and 4,096 random elements of every expert), the
 whole output checked for unwritten / non-finite elements, bit-reproducibility
 over two runs, and exact zeros for empty experts."""
 import numpy as np
@@ -46,7 +47,7 @@ def test_workload_parity(name):
         assert not out[g].view(torch.int16).any(), f"empty expert {g} not exact +0"
 
     rng = np.random.default_rng(w.seed)
-    g, n, k = sample_indices(w.E, w.N, w.K, rng)
+    g, n, k = sample_indices(w.E, w.N, w.K, rng, tiling=mx.tile_config(w.E, w.N, w.K, w.M))
     keep = sizes[g] > 0
     g, n, k = g[keep], n[keep], k[keep]
     ref, _, aacc = oracle.wgrad_points(A, sA, B, sB, offs, w.E, w.N, w.K, w.M, g, n, k, want_acc=True)
