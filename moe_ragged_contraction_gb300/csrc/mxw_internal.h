@@ -30,8 +30,14 @@ constexpr int PLAN_HDR = 8;
 // chunk (n1 = min(tn, 256)); nblk_n = ceil(tn / 128) scale blocks per N-side
 // tile; tiles_m = ceil(rows of the M side / 256), tiles_n = ceil(rows of the
 // N side / tn).
+// m_fastest: the order of one expert's tiles in the schedule (weight
+// gradient). A pass of the persistent grid covers a run of consecutive tiles,
+// so the operand indexed by the faster-moving tile index is read in full by
+// every pass over the expert while the other is read about once: the faster
+// index runs over the side with fewer rows (1: the M side, else the N side).
 struct TileConfig {
     int kn, tn, n1, n2, nblk_n, tiles_m, tiles_n;
+    int m_fastest;
 };
 
 // force: 0 = the orientation the kernel's cost model prefers (ties: kn == 0),

@@ -46,7 +46,12 @@
 // 1: tiles wider than 256 columns (two MMAs per 32-token chunk, one A tile)
 // read A from shared memory once per chunk through the collector buffer.
 #ifndef MXW_COLLECTOR_A
-#define MXW_COLLECTOR_A 0
+#define MXW_COLLECTOR_A 1
+#endif
+// Order of an expert's tiles: -1 the side with fewer rows fastest, 0 the N
+// side's tiles fastest, 1 the M side's.
+#ifndef MXW_ORDER
+#define MXW_ORDER -1
 #endif
 
 namespace mxw {
@@ -559,6 +564,7 @@ struct MainParams {
     int tn, n1, n2;          // N-side tile rows = n1 + n2 (the two MMA widths; n2 may be 0)
     int nblk_n;              // 128-row scale blocks per N-side tile
     int kn;                  // 0: M side = rows of A (n), N side = rows of B (k); 1: swapped
+    int m_fastest;           // mode 0: an expert's tiles ordered M-side tile fastest (else N-side tile fastest)
     int stages, sf_slots;
     int acc_bufs;            // accumulators in TMEM (2: the next tile's MMAs overlap this tile's drain)
     int wide_stores;         // 32-byte output stores (rows of 16 columns 32-byte aligned), else 16-byte
@@ -626,8 +632,13 @@ __device__ __forceinline__ Item load_item(const MainParams& p, long long i) {
         const int r = static_cast<int>(i / ntpe);
         const int t = static_cast<int>(i - static_cast<long long>(r) * ntpe);
         it.g = __ldg(order + r);
-        it.tm = t / p.tiles_n;
-        it.tn = t - it.tm * p.tiles_n;
+        if (p.m_fastest) {
+            it.tn = t / p.tiles_m;
+            it.tm = t - it.tn * p.tiles_m;
+        } else {
+            it.tm = t / p.tiles_n;
+            it.tn = t - it.tm * p.tiles_n;
+        }
         it.start = __ldg(ex + 4 * it.g + 0);
         it.len = __ldg(ex + 4 * it.g + 1);
         it.nsteps = __ldg(ex + 4 * it.g + 2);
@@ -756,41 +767,45 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
         }
         tc_fence_after();
         const uint32_t acc_t = tmem + buf * acc_cols;
+        // scale factors of stage `stg` into TMEM slot `slt`
+        auto copy_sf = [&](uint32_t stg, uint32_t slt) {
+            const uint32_t sfa_t = sf_tmem0 + slt * SF_COLS;
+            tc_cp_32x128b_warpx4_pair_elect(sfa_t, desc_sf_block(sfa_s0 + stg * SF_ATOM));
+#pragma unroll
+            for (int b = 0; b < NBLK; ++b)
+                tc_cp_32x128b_warpx4_pair_elect(sfa_t + 4 + 4 * b, desc_sf_block(sfb_s0 + stg * SFB_STAGE + b * SF_ATOM));
+        };
+        // the MMAs of 32-token chunk kk of K-step s from stage stg, scales in slot slt
+        auto mma_chunk = [&](int s, int kk, uint32_t stg, uint32_t slt) {
+            const uint32_t sfa_t = sf_tmem0 + slt * SF_COLS;
+            const uint32_t sfb_t = sfa_t + 4;
+            const uint32_t a_s = a_s0 + stg * A_STAGE;
+            const uint32_t b_s = b_s0 + stg * b_stage;
+            const uint32_t sel = (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
+            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t ad = desc_kmajor_sw128(a_s + 32 * kk);
+            if (TWO && MXW_COLLECTOR_A) {
+                // both MMAs of the chunk multiply the same A tile: the
+                // second reads it from the collector buffer
+                tc_mma_mxf8_pair_elect_fill(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t,
+                                            acc);
+                tc_mma_mxf8_pair_elect_lastuse(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk),
+                                               idesc2 | sel, sfa_t, sfb_t + 8, acc);
+            } else {
+                tc_mma_mxf8_pair_elect(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t, acc);
+                if (TWO)
+                    tc_mma_mxf8_pair_elect(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk), idesc2 | sel,
+                                           sfa_t, sfb_t + 8, acc);
+            }
+        };
         for (int s = 0; s < it.nsteps; ++s, ++c) {
             named_bar_sync(BAR_READY + st, 64);
             if (live) {
                 tc_fence_after();
-                const uint32_t sfa_t = sf_tmem0 + slot * SF_COLS;
-                const uint32_t sfb_t = sfa_t + 4;
-                const uint32_t sfa_s = sfa_s0 + st * SF_ATOM;
-                const uint32_t sfb_s = sfb_s0 + st * SFB_STAGE;
-                tc_cp_32x128b_warpx4_pair_elect(sfa_t, desc_sf_block(sfa_s));
-#pragma unroll
-                for (int b = 0; b < NBLK; ++b)
-                    tc_cp_32x128b_warpx4_pair_elect(sfb_t + 4 * b, desc_sf_block(sfb_s + b * SF_ATOM));
+                copy_sf(st, slot);
                 const int rem = it.len - s * BK;
                 const int nk = rem >= BK ? 4 : (rem >> 5);
-                const uint32_t a_s = a_s0 + st * A_STAGE;
-                const uint32_t b_s = b_s0 + st * b_stage;
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t sel = (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
-                    const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                    const uint64_t ad = desc_kmajor_sw128(a_s + 32 * kk);
-                    if (TWO && MXW_COLLECTOR_A) {
-                        // both MMAs of the chunk multiply the same A tile: the
-                        // second reads it from the collector buffer
-                        tc_mma_mxf8_pair_elect_fill(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t,
-                                                    sfb_t, acc);
-                        tc_mma_mxf8_pair_elect_lastuse(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk),
-                                                       idesc2 | sel, sfa_t, sfb_t + 8, acc);
-                    } else {
-                        tc_mma_mxf8_pair_elect(acc_t, ad, desc_kmajor_sw128(b_s + 32 * kk), idesc1 | sel, sfa_t, sfb_t,
-                                               acc);
-                        if (TWO)
-                            tc_mma_mxf8_pair_elect(acc_t + 256, ad, desc_kmajor_sw128(b_s + B2_OFF + 32 * kk),
-                                                   idesc2 | sel, sfa_t, sfb_t + 8, acc);
-                    }
-                }
+                for (int kk = 0; kk < nk; ++kk) mma_chunk(s, kk, st, slot);
                 tc_commit_pair_elect(x.bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
             }
             named_bar_arrive(BAR_FREE + st, 64);
@@ -1325,6 +1340,7 @@ TileConfig make_config(int kn, int tn, int rows_m, int rows_n) {
     tc.nblk_n = (tn + 127) / 128;
     tc.tiles_m = (rows_m + PAIR_M - 1) / PAIR_M;
     tc.tiles_n = (rows_n + tn - 1) / tn;
+    tc.m_fastest = MXW_ORDER >= 0 ? MXW_ORDER : (rows_m < rows_n ? 1 : 0);
     return tc;
 }
 
@@ -1539,6 +1555,7 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     mp.n2 = tc.n2;
     mp.nblk_n = tc.nblk_n;
     mp.kn = tc.kn;
+    mp.m_fastest = mp.mode == 0 ? tc.m_fastest : 0;
     mp.stages = geo.stages;
     mp.sf_slots = geo.sf_slots;
     mp.acc_bufs = geo.acc_bufs;
