@@ -460,6 +460,12 @@ def bench_gpu(args):
     else:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": peak_src, "algorithmic_flop_per_launch": flop}
+        if peaks and "bf16_tflops_sustained" in peaks:
+            # context: the timed steps follow 0.5 s of back-to-back calls, so the
+            # large shapes run at the clock the 1.4 kW cap allows; the measured
+            # sustained bf16 figure (4 s back to back) x 2 is that regime's peak
+            ps = FP8_OVER_BF16 * float(peaks["bf16_tflops_sustained"])
+            roof.update({"peak_sustained": ps, "frac_sustained": achieved / ps})
     roof.update({"traffic": traffic, "kernel": "wgrad_main", "avg_launch_ms": main_avg})
 
     result = None
@@ -514,7 +520,11 @@ def bench_comparators(args):
     against a BF16 grouped GEMM, "Ragged MXFP8 Weight Gradients" section 7),
     and a dense 8192^3 MXFP8 GEMM through this library (one expert) and
     through cuBLASLt (torch._scaled_mm with e8m0 block scales; its scales are
-    not in the vendor's swizzled layout, so only its timing is meaningful)."""
+    not in the vendor's swizzled layout, so only its timing is meaningful).
+    Each is timed two ways in the same process: "burst" (steps after three
+    warm-ups, L2 flushed before each) and "sustained" (three passes of at
+    least one second of back-to-back calls each, the regime in which the
+    1.4 kW power cap sets the clock; median, minimum, maximum)."""
     import torch
 
     import moe_ragged_contraction_gb300 as mx
@@ -540,11 +550,35 @@ def bench_comparators(args):
             tot += a.elapsed_time(b)
         return tot / steps
 
-    res = {"comparators": True, "config": {"workload": args.config}, "unit": "TFLOP/s"}
+    def sustained(fn, flop_per_call, seconds=1.0, passes=3):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(3):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        calls = int(max(5, np.ceil(seconds / max(1e-6, a.elapsed_time(b) / 3 * 1e-3))))
+        vals = []
+        for _ in range(passes):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(calls):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            vals.append(flop_per_call / (a.elapsed_time(b) / calls * 1e-3) / 1e12)
+        return dict(spread(vals), calls_per_pass=calls)
+
+    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(device).uuid))
+    sampler.start()
+    res = {"comparators": True, "config": {"workload": args.config}, "unit": "TFLOP/s", "sustained": {}}
     A, sA, B, sB, offs = make_device_inputs(args.config, device)
     out = torch.empty((w.E, w.N, w.K), dtype=torch.bfloat16, device=device)
-    ms = timed(lambda: mx.wgrad_grouped(A, sA, B, sB, offs, out=out), args.steps)
+    ours = lambda: mx.wgrad_grouped(A, sA, B, sB, offs, out=out)  # noqa: E731
+    ms = timed(ours, args.steps)
     res["mxfp8_wgrad_this_library"] = w.flop / (ms * 1e-3) / 1e12
+    res["sustained"]["mxfp8_wgrad_this_library"] = sustained(ours, w.flop)
     # BF16 vendor baseline: one cuBLAS bf16 GEMM per expert on the token slice
     # (torch._grouped_mm is not used: it raised a GPU fault in one run on
     # this hardware)
@@ -564,7 +598,11 @@ def bench_comparators(args):
 
     ms = timed(bf16_loop, args.steps)
     res["bf16_per_expert_cublas"] = w.flop / (ms * 1e-3) / 1e12
+    res["sustained"]["bf16_per_expert_cublas"] = sustained(bf16_loop, w.flop)
     res["mxfp8_over_bf16"] = res["mxfp8_wgrad_this_library"] / res["bf16_per_expert_cublas"]
+    res["mxfp8_over_bf16_sustained"] = (res["sustained"]["mxfp8_wgrad_this_library"]["median"]
+                                        / res["sustained"]["bf16_per_expert_cublas"]["median"])
+    del a16, b16, out16
     n = 8192
     g = torch.Generator(device=device)
     g.manual_seed(0)
@@ -572,16 +610,22 @@ def bench_comparators(args):
     qb, qsb = mx.quantize_tokenwise(torch.randn(n, n, device=device, generator=g))
     one = torch.tensor([n], dtype=torch.int32, device=device)
     dout = torch.empty((1, n, n), dtype=torch.bfloat16, device=device)
-    ms = timed(lambda: mx.wgrad_grouped(qa, qsa, qb, qsb, one, out=dout), args.steps)
+    dense_ours = lambda: mx.wgrad_grouped(qa, qsa, qb, qsb, one, out=dout)  # noqa: E731
+    ms = timed(dense_ours, args.steps)
     res["dense8192_mxfp8_this_library"] = 2 * n ** 3 / (ms * 1e-3) / 1e12
+    res["sustained"]["dense8192_mxfp8_this_library"] = sustained(dense_ours, 2.0 * n ** 3)
     try:
         a8, b8 = qa.view(torch.float8_e4m3fn), qb.view(torch.float8_e4m3fn).t()
         s_a, s_b = qsa.view(torch.float8_e8m0fnu), qsb.view(torch.float8_e8m0fnu)
-        ms = timed(lambda: torch._scaled_mm(a8, b8, scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16), args.steps)
+        vendor = lambda: torch._scaled_mm(a8, b8, scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16)  # noqa: E731
+        ms = timed(vendor, args.steps)
         res["dense8192_mxfp8_vendor"] = 2 * n ** 3 / (ms * 1e-3) / 1e12
+        res["sustained"]["dense8192_mxfp8_vendor"] = sustained(vendor, 2.0 * n ** 3)
     except Exception as e:
         res["dense8192_mxfp8_vendor"] = None
         res["dense8192_vendor_error"] = str(e).splitlines()[0][:200]
+    res["clocks"] = sampler.stop()
+    res["gpu_launches_note"] = "context line, not a bench line"
     return res
 
 
