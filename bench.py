@@ -691,6 +691,129 @@ def bench_quantizer(args):
             "gpu_launches": 2 * K, "clocks": clocks}
 
 
+# ------------------------------------------------------------------ scale-factor blocks from the quantiser
+
+def bench_sf(args):
+    """Opt-in line: the operands quantised from token-major bf16 by the fused
+    quantiser that writes the scales straight into the tensor core's block
+    layout, then the weight gradient over those blocks (no scale re-layout
+    inside the timed call). Same metric, workload, flush and step protocol as
+    the default line; the quantiser is timed separately (GB/s)."""
+    import torch
+
+    import moe_ragged_contraction_gb300 as mx
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    mx.build()
+    mx.load()
+    w = I.WORKLOADS[args.config]
+    cfg = mx.tile_config(w.E, w.N, w.K, w.M)
+    kn, tn = cfg["kn"], cfg["tn"]
+    rows_a, rows_b = (tn, 256) if kn else (256, tn)
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    dy = torch.randn(w.M, w.N, device=device, generator=g).to(torch.bfloat16)
+    x = torch.randn(w.M, w.K, device=device, generator=g).to(torch.bfloat16)
+    A = torch.empty((w.N, w.M), dtype=torch.uint8, device=device)
+    B = torch.empty((w.K, w.M), dtype=torch.uint8, device=device)
+    sfA = torch.empty((mx.sf_blocks_bytes(w.N, w.M, rows_a),), dtype=torch.uint8, device=device)
+    sfB = torch.empty((mx.sf_blocks_bytes(w.K, w.M, rows_b),), dtype=torch.uint8, device=device)
+    offs = torch.from_numpy(I.offsets(I.group_sizes(args.config))).to(device)
+    out = torch.empty((w.E, w.N, w.K), dtype=torch.bfloat16, device=device)
+    flush = L2Flush(device)
+    stream = torch.cuda.current_stream(device)
+
+    def quant():
+        mx.quantize_transpose_bf16_sf(dy, rows_a, q=A, sf=sfA)
+        mx.quantize_transpose_bf16_sf(x, rows_b, q=B, sf=sfB)
+
+    def step(pair=None):
+        if pair is not None:
+            mx.set_timing_events(*pair)
+        mx.wgrad_grouped_sf(A, sfA, B, sfB, offs, kn, tn, out=out)
+
+    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(device).uuid))
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        flush()
+        quant()
+    torch.cuda.synchronize()
+    K = args.steps
+    evq = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    hold_gpu(K)
+    for i in range(K):
+        flush()
+        evq[i][0].record(stream)
+        quant()
+        evq[i][1].record(stream)
+    torch.cuda.synchronize()
+    q_ms = float(np.mean([a.elapsed_time(b) for a, b in evq]))
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in evm:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    hold_gpu(K)
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    hold_gpu(K)
+    for i in range(K):
+        flush()
+        step(pair=evm[i])
+    torch.cuda.synchronize()
+    main_ms = float(np.mean([a.elapsed_time(b) for a, b in evm]))
+    calls = int(max(10, np.ceil(1.0 / max(1e-6, float(np.mean(step_ms)) * 1e-3))))
+    b2b = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_gpu(min(calls, 200))
+        e0.record(stream)
+        for _ in range(calls):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        b2b.append(float(w.flop) / (e0.elapsed_time(e1) / calls * 1e-3) / 1e12)
+    clocks = sampler.stop()
+    assert mx.device_status(clear=True) == 0, "device flagged an error during the benchmark"
+    flop = float(w.flop)
+    peak, peak_src, peaks = mxfp8_peak()
+    ms = float(np.mean(step_ms))
+    elems = float(w.M) * (w.N + w.K)
+    q_bytes = elems * (2 + 1) + float(sfA.numel() + sfB.numel())
+    hbm = float(peaks["hbm_gbs"]) if peaks else HBM_FALLBACK_GBS
+    return {"metric": METRIC + ", scales laid out by the quantiser", "value": flop / (ms * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "ms_per_step": ms, "steps": K, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "mxfp8_e4m3 (e8m0 block-32 scales), fp32 accumulate, bf16 out",
+            "data": "synthetic (seeded routing, N(0,1) bf16 operands quantised on the GPU)",
+            "config": dict(bench_config(args.config, 1), tiling={"kn": kn, "tn": tn}),
+            "spread": {"unit": "TFLOP/s", "timed_steps": spread([flop / (t * 1e-3) / 1e12 for t in step_ms]),
+                       "back_to_back": dict(spread(b2b), calls_per_pass=calls)},
+            "roofline": {"bound": "tensor", "achieved": flop / (main_ms * 1e-3) / 1e12, "peak": peak,
+                         "unit": "TFLOP/s", "frac": flop / (main_ms * 1e-3) / 1e12 / peak, "peak_source": peak_src,
+                         "kernel": "wgrad_main (grid K-steps, caller's scale blocks)", "avg_launch_ms": main_ms},
+            "quantizer": {"ms_per_step": q_ms, "unit": "GB/s", "value": q_bytes / (q_ms * 1e-3) / 1e9,
+                          "frac_of_hbm": q_bytes / (q_ms * 1e-3) / 1e9 / hbm,
+                          "what": "both operands, bf16 [M, R] -> E4M3 [R, M] + scale blocks, L2 flushed"},
+            "gpu_launches": 2 * K, "clocks": clocks}
+
+
 # ------------------------------------------------------------------ grouped GEMM (forward / data gradient)
 
 def _rowwise_mxfp8(rows: int, cols: int, seed: int, stream: int, dist: str, device):
@@ -891,6 +1014,8 @@ def main():
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only: no settle loop, spread passes, end-to-end leg or CPU "
                          "baseline (profiler runs)")
+    ap.add_argument("--sf", action="store_true",
+                    help="print a line for the weight gradient over scale blocks written by the quantiser instead")
     ap.add_argument("--gemm", action="store_true",
                     help="print a line for the layer's forward and data-gradient grouped GEMMs (ragged rows) instead")
     args = ap.parse_args()
@@ -906,6 +1031,8 @@ def main():
         res = bench_quantizer(args)
     elif args.gemm:
         res = bench_gemm(args)
+    elif args.sf:
+        res = bench_sf(args)
     else:
         res = bench_reference_arm(args) if args.impl == "reference" else bench_gpu(args)
     if res is not None:

@@ -184,6 +184,54 @@ int mxfp8_grouped_gemm_tile_config(int E, int N, int K, int64_t M, int* tn, int*
  */
 int mxfp8_quantize_transpose_bf16(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s, void* stream);
 
+/*
+ * Scale factors written straight into the tensor core's layout ("Ragged MXFP8
+ * Weight Gradients", section 5.6: the scale planes are pre-shuffled into the
+ * form the matrix instruction reads; here the quantiser writes that form, so
+ * the weight gradient below needs no re-layout pass).
+ *
+ * Layout ("SF blocks") for a [R][M] operand cut into tiles of `tile_rows` rows
+ * and into 128-token steps on the global token grid: one 512-byte block per
+ * (tile t, step g, 128-row block h of the tile), stored at
+ *   ((t * ceil(M/128) + g) * ceil(tile_rows/128) + h) * 512,
+ * holding tile row 128 h + r (r < 128) and 32-token block kb (kb < 4) of step
+ * g at byte (r % 32) * 16 + (r / 32) * 4 + kb. Rows past R and tokens past M
+ * hold 0x00.
+ *
+ * mxfp8_sf_blocks_bytes gives the size: ceil(R/tile_rows) * ceil(M/128) *
+ * ceil(tile_rows/128) * 512 (0 for invalid sizes: R >= 1, M >= 32,
+ * M % 32 == 0, tile_rows a positive multiple of 16). Host-only.
+ */
+size_t mxfp8_sf_blocks_bytes(int R, int64_t M, int tile_rows);
+
+/*
+ * mxfp8_quantize_transpose_bf16 that also writes the scales as SF blocks for
+ * tiles of `tile_rows` rows (sf, mxfp8_sf_blocks_bytes(R, M, tile_rows) bytes,
+ * every byte written); s may be NULL (no row-major plane). Arguments,
+ * rounding and alignment otherwise as mxfp8_quantize_transpose_bf16.
+ */
+int mxfp8_quantize_transpose_bf16_sf(const uint16_t* x, int64_t M, int R, int tile_rows, uint8_t* q, uint8_t* s,
+                                     uint8_t* sf, void* stream);
+
+/*
+ * The weight gradient of mxfp8_wgrad_grouped with the scales given as SF
+ * blocks (no scale re-layout inside the call; the plan of the runs is still
+ * built from offs on the device). The caller picks the tiling and lays the
+ * scales out for it: kn = 0 puts the pair tile's 256-row side on A and tn
+ * rows on B, kn = 1 the reverse (mxfp8_wgrad_tile_config reports the
+ * library's choice); sfA holds A's scales as SF blocks for tiles of
+ * (kn ? tn : 256) rows and sfB B's for tiles of (kn ? 256 : tn) rows, both
+ * 16-byte aligned. tn is a multiple of 16 in [16, 448] (MXFP8_EINVAL
+ * otherwise). Each expert's K-steps run on the 128-token grid: a run that
+ * starts inside a step skips that step's leading 32-token chunks, so every
+ * output element sums the same 32-token block products in the same order as
+ * mxfp8_wgrad_grouped: the results are the same bits. Other arguments,
+ * preconditions, scratch (the plan only) and errors as mxfp8_wgrad_grouped.
+ */
+int mxfp8_wgrad_grouped_sf(const uint8_t* A, const uint8_t* sfA, const uint8_t* B, const uint8_t* sfB,
+                           const int32_t* offs, int E, int N, int K, int64_t M, int kn, int tn, uint16_t* out,
+                           void* stream);
+
 /* Message for the last non-zero status returned on the calling thread
  * (thread-local; never NULL). */
 const char* mxfp8_last_error(void);

@@ -16,12 +16,15 @@ from ._lib import (  # noqa: F401
     load,
     quantize_tokenwise,
     quantize_transpose_bf16,
+    quantize_transpose_bf16_sf,
     set_epilogue_store,
     set_tile_orientation,
     set_tile_rows,
     set_timing_events,
+    sf_blocks_bytes,
     tile_config,
     wgrad_grouped,
+    wgrad_grouped_sf,
     workspace_bytes,
 )
 from .build import build  # noqa: F401

@@ -64,6 +64,12 @@ def load() -> ctypes.CDLL:
         lib.mxfp8_grouped_gemm.restype = I
         lib.mxfp8_quantize_transpose_bf16.argtypes = [P, L, I, P, P, P]
         lib.mxfp8_quantize_transpose_bf16.restype = I
+        lib.mxfp8_quantize_transpose_bf16_sf.argtypes = [P, L, I, I, P, P, P, P]
+        lib.mxfp8_quantize_transpose_bf16_sf.restype = I
+        lib.mxfp8_sf_blocks_bytes.argtypes = [I, L, I]
+        lib.mxfp8_sf_blocks_bytes.restype = Z
+        lib.mxfp8_wgrad_grouped_sf.argtypes = [P, P, P, P, P, I, I, I, L, I, I, P, P]
+        lib.mxfp8_wgrad_grouped_sf.restype = I
         lib.mxfp8_last_error.argtypes = []
         lib.mxfp8_last_error.restype = ctypes.c_char_p
         lib.mxfp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), I]
@@ -251,6 +257,66 @@ def quantize_transpose_bf16(x, q=None, s=None, stream=None):
         raise ValueError(f"q must be [{R}, {M}] and s [{R}, {M // 32}]")
     check(load().mxfp8_quantize_transpose_bf16(_ptr(x), M, R, _ptr(q), _ptr(s), _stream(stream)))
     return q, s
+
+
+def sf_blocks_bytes(R: int, M: int, tile_rows: int) -> int:
+    """Bytes of the scale-factor blocks of an [R, M] operand cut into tiles of tile_rows rows (0 if invalid)."""
+    return int(load().mxfp8_sf_blocks_bytes(R, M, tile_rows))
+
+
+def quantize_transpose_bf16_sf(x, tile_rows, q=None, sf=None, s=None, stream=None):
+    """Fused quantise-and-transpose writing the scales as tcgen05 scale-factor
+    blocks for tiles of ``tile_rows`` rows (see include/mxfp8_wgrad.h):
+    x bf16 [M, R] -> (q uint8 [R, M] E4M3, sf uint8 [sf_blocks_bytes(R, M, tile_rows)],
+    s uint8 [R, M/32] or None when not asked for)."""
+    import torch
+
+    _expect(x, torch.bfloat16, "x")
+    M, R = x.shape
+    nbytes = sf_blocks_bytes(R, M, tile_rows)
+    if nbytes == 0:
+        raise ValueError(f"invalid sizes R={R}, M={M}, tile_rows={tile_rows}")
+    if q is None:
+        q = torch.empty((R, M), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty((nbytes,), dtype=torch.uint8, device=x.device)
+    _expect(q, torch.uint8, "q")
+    _expect(sf, torch.uint8, "sf")
+    if s is not None:
+        _expect(s, torch.uint8, "s")
+        if tuple(s.shape) != (R, M // 32):
+            raise ValueError(f"s must be [{R}, {M // 32}]")
+    if tuple(q.shape) != (R, M) or sf.numel() < nbytes:
+        raise ValueError(f"q must be [{R}, {M}] and sf hold {nbytes} bytes")
+    check(load().mxfp8_quantize_transpose_bf16_sf(_ptr(x), M, R, int(tile_rows), _ptr(q), _ptr(s), _ptr(sf),
+                                                  _stream(stream)))
+    return q, sf, s
+
+
+def wgrad_grouped_sf(A, sfA, B, sfB, offs, kn, tn, out=None, stream=None):
+    """The weight gradient with scales given as scale-factor blocks laid out
+    for the tiling (kn, tn) (see include/mxfp8_wgrad.h): sfA for tiles of
+    (tn if kn else 256) rows of A, sfB for tiles of (256 if kn else tn) rows of B.
+    A: uint8 [N, M], B: uint8 [K, M], offs: int32 [E]. Returns (or fills) out bf16 [E, N, K]."""
+    import torch
+
+    for t, dt, nm in ((A, torch.uint8, "A"), (sfA, torch.uint8, "sfA"), (B, torch.uint8, "B"),
+                      (sfB, torch.uint8, "sfB"), (offs, torch.int32, "offs")):
+        _expect(t, dt, nm)
+    N, M = A.shape
+    K, M2 = B.shape
+    E = offs.numel()
+    rows_a, rows_b = (int(tn), 256) if kn else (256, int(tn))
+    if M2 != M or sfA.numel() < sf_blocks_bytes(N, M, rows_a) or sfB.numel() < sf_blocks_bytes(K, M, rows_b):
+        raise ValueError("inconsistent operand / scale-factor block sizes")
+    if out is None:
+        out = torch.empty((E, N, K), dtype=torch.bfloat16, device=A.device)
+    _expect(out, torch.bfloat16, "out")
+    if tuple(out.shape) != (E, N, K):
+        raise ValueError(f"out must be [{E}, {N}, {K}]")
+    check(load().mxfp8_wgrad_grouped_sf(_ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB), _ptr(offs), E, N, K, M, int(kn),
+                                        int(tn), _ptr(out), _stream(stream)))
+    return out
 
 
 def device_status(clear: bool = True) -> int:

@@ -262,8 +262,16 @@ int validate(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_
     return MXFP8_OK;
 }
 
+// Scale factors the caller already laid out as tcgen05 blocks on the global
+// 128-token grid (mxfp8_wgrad_grouped_sf), with the tiling they were laid out for.
+struct SfUser {
+    const uint8_t *sfA, *sfB;
+    int kn, tn;
+};
+
 int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const int32_t* offs, int E, int N,
-        int K, int64_t M, uint16_t* out, void* ws, size_t ws_bytes, bool use_cache, void* stream) {
+        int K, int64_t M, uint16_t* out, void* ws, size_t ws_bytes, bool use_cache, void* stream,
+        const SfUser* sfu = nullptr) {
     cudaEvent_t evb = g_ev_before, eva = g_ev_after;
     g_ev_before = g_ev_after = nullptr;
     const int stall = g_stall_next;
@@ -273,9 +281,26 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     if (E == 0) return MXFP8_OK;
     mxw::TileConfig tc;
     mxw::WsLayout lay;
-    if (!mxw::choose_tiles(N, K, E, M, orientation_mode(), tile_rows_setting(), &tc) ||
-        !mxw::ws_layout(E, N, K, M, tc, &lay))
+    if (sfu) {
+        if (sfu->kn != 0 && sfu->kn != 1) return fail(MXFP8_EINVAL, "kn=%d must be 0 or 1", sfu->kn);
+        if (!mxw::choose_tiles(N, K, E, M, sfu->kn + 1, sfu->tn, &tc))
+            return fail(MXFP8_EINVAL, "tile rows tn=%d: a multiple of 16 in [16, %d]", sfu->tn, mxw::MAX_TN);
+        if (!aligned16(sfu->sfA) || !aligned16(sfu->sfB))
+            return fail(MXFP8_EALIGN, "sfA and sfB must be 16-byte aligned");
+        const int64_t steps = (M + mxw::BK - 1) / mxw::BK;
+        const int64_t rows_m = static_cast<int64_t>(tc.tiles_m) * steps * 2;
+        const int64_t rows_n = static_cast<int64_t>(tc.tiles_n) * steps * tc.nblk_n;
+        if (rows_m > (int64_t(1) << 31) - 1 || rows_n > (int64_t(1) << 31) - 1 ||
+            static_cast<int64_t>(E) * tc.tiles_m * tc.tiles_n > (int64_t(1) << 31) - 1)
+            return fail(MXFP8_EINVAL, "unsupported sizes");
+        lay.tc = tc;
+        lay.ts_max = static_cast<int>(steps);
+        lay.plan_off = lay.sfm_off = lay.sfn_off = 0;
+        lay.total = sizeof(int32_t) * (mxw::PLAN_HDR + 5 * static_cast<size_t>(E));
+    } else if (!mxw::choose_tiles(N, K, E, M, orientation_mode(), tile_rows_setting(), &tc) ||
+               !mxw::ws_layout(E, N, K, M, tc, &lay)) {
         return fail(MXFP8_EINVAL, "unsupported sizes");
+    }
     if (!use_cache) {
         if (!ws) return fail(MXFP8_EINVAL, "null workspace");
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MXFP8_EALIGN, "workspace must be 256-byte aligned");
@@ -321,10 +346,12 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     if (rc) return rc;
     rc = make_operand_map3(&maps[2], n_op, M, n_rows, 1, tc.n2 ? tc.n2 / 2 : tc.n1 / 2);
     if (rc) return rc;
-    rc = make_sf_map(&maps[3], static_cast<uint8_t*>(ws) + lay.sfm_off, static_cast<int64_t>(tc.tiles_m) * lay.ts_max * 2, 1);
+    // scale-factor blocks: the prep's re-layout in the workspace, or the caller's
+    const uint8_t* sf_m = sfu ? (tc.kn ? sfu->sfB : sfu->sfA) : static_cast<uint8_t*>(ws) + lay.sfm_off;
+    const uint8_t* sf_n = sfu ? (tc.kn ? sfu->sfA : sfu->sfB) : static_cast<uint8_t*>(ws) + lay.sfn_off;
+    rc = make_sf_map(&maps[3], sf_m, static_cast<int64_t>(tc.tiles_m) * lay.ts_max * 2, 1);
     if (rc) return rc;
-    rc = make_sf_map(&maps[4], static_cast<uint8_t*>(ws) + lay.sfn_off,
-                     static_cast<int64_t>(tc.tiles_n) * lay.ts_max * tc.nblk_n, tc.nblk_n);
+    rc = make_sf_map(&maps[4], sf_n, static_cast<int64_t>(tc.tiles_n) * lay.ts_max * tc.nblk_n, tc.nblk_n);
     if (rc) return rc;
 
     mxw::WgradArgs a;
@@ -339,6 +366,7 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     a.ev_before = evb;
     a.ev_after = eva;
     a.stall_first_stage = stall;
+    a.grid = sfu ? 1 : 0;
     // output as [E][N][K] for the TMA-store epilogue (used where its staging fits)
     a.tma_store = (store_mode() == 0 && make_out_map(&maps[5], out, K, N, E)) ? 1 : 0;
     if (!a.tma_store) maps[5] = maps[0];
@@ -398,6 +426,21 @@ int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B
                            const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out, void* workspace,
                            size_t workspace_bytes, void* stream) {
     return run(A, sA, B, sB, offs, E, N, K, M, out, workspace, workspace_bytes, false, stream);
+}
+
+int mxfp8_wgrad_grouped_sf(const uint8_t* A, const uint8_t* sfA, const uint8_t* B, const uint8_t* sfB,
+                           const int32_t* offs, int E, int N, int K, int64_t M, int kn, int tn, uint16_t* out,
+                           void* stream) {
+    const SfUser sfu{sfA, sfB, kn, tn};
+    return run(A, sfA, B, sfB, offs, E, N, K, M, out, nullptr, 0, true, stream, &sfu);
+}
+
+size_t mxfp8_sf_blocks_bytes(int R, int64_t M, int tile_rows) {
+    if (R < 1 || M < 32 || (M % 32) != 0 || tile_rows < 16 || (tile_rows % 16) != 0) return 0;
+    const size_t tiles = (static_cast<size_t>(R) + tile_rows - 1) / tile_rows;
+    const size_t steps = (static_cast<size_t>(M) + mxw::BK - 1) / mxw::BK;
+    const size_t nblk = (static_cast<size_t>(tile_rows) + 127) / 128;
+    return tiles * steps * nblk * mxw::SF_ATOM;
 }
 
 int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, void* stream) {
@@ -500,6 +543,27 @@ int mxfp8_quantize_transpose_bf16(const uint16_t* x, int64_t M, int R, uint8_t* 
     int rc = current_device(&dev, &info);
     if (rc) return rc;
     cudaError_t e = mxw::launch_quantize_transpose(x, M, R, q, s, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "quantize-transpose kernel");
+    return MXFP8_OK;
+}
+
+int mxfp8_quantize_transpose_bf16_sf(const uint16_t* x, int64_t M, int R, int tile_rows, uint8_t* q, uint8_t* s,
+                                     uint8_t* sf, void* stream) {
+    if (R < 1) return fail(MXFP8_EINVAL, "R=%d must be >= 1", R);
+    if (M < 32 || (M % 32) != 0) return fail(MXFP8_EINVAL, "M=%lld must be a positive multiple of 32", (long long)M);
+    if (tile_rows < 16 || (tile_rows % 16) != 0)
+        return fail(MXFP8_EINVAL, "tile_rows=%d must be a positive multiple of 16", tile_rows);
+    if (!x || !q || !sf) return fail(MXFP8_EINVAL, "null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(x) & 1u) != 0) return fail(MXFP8_EALIGN, "x must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return fail(MXFP8_EALIGN, "q must be 16-byte aligned");
+    const int64_t rows = ((static_cast<int64_t>(R) + tile_rows - 1) / tile_rows) * tile_rows;
+    if (M / 64 + 1 > 0x7fffffffLL || (rows + 127) / 128 > 65535 || rows > 0x7fffffffLL)
+        return fail(MXFP8_EINVAL, "M=%lld, R=%d: too large", (long long)M, R);
+    int dev;
+    DeviceInfo info;
+    int rc = current_device(&dev, &info);
+    if (rc) return rc;
+    cudaError_t e = mxw::launch_quantize_transpose_sf(x, M, R, q, s, sf, tile_rows, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "quantize-transpose kernel");
     return MXFP8_OK;
 }

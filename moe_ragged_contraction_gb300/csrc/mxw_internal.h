@@ -75,6 +75,8 @@ struct WgradArgs {
     cudaEvent_t ev_before, ev_after;
     int stall_first_stage;  // failure-path test hook (0 in normal use)
     int tma_store;          // maps[5] describes out: TMA-store epilogue where its staging fits
+    int grid;               // 1: K-steps on the global 128-token grid, scale blocks given by the
+                            // caller (maps[3], maps[4]; lay.ts_max = grid steps); the prep writes the plan only
 };
 
 // Enqueue the plan / scale re-layout kernel and the main contraction kernel.
@@ -121,6 +123,11 @@ cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap* maps, const char**
 cudaError_t launch_quantize(const float* x, int R, int64_t M, uint8_t* q, uint8_t* s, cudaStream_t stream);
 cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s,
                                       cudaStream_t stream);
+// As launch_quantize_transpose, writing the scales also (or only: s may be
+// null) as tcgen05 scale-factor blocks for tiles of tile_rows rows on the
+// global 128-token grid (sf: [ceil(R / tile_rows)][ceil(M / 128)][ceil(tile_rows / 128)][512 B]).
+cudaError_t launch_quantize_transpose_sf(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s, uint8_t* sf,
+                                         int tile_rows, cudaStream_t stream);
 
 // Loads the module holding the weight-gradient kernels on the current device
 // (the runtime otherwise loads it at the first launch), without launching.

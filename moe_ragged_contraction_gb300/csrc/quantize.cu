@@ -106,10 +106,35 @@ constexpr int QX_THREADS = 256;
 
 __device__ __forceinline__ int qx_piece(int row, int p) { return p ^ (row & 7) ^ ((row >> 3) & 7); }
 
+// Scale-factor block output of the quantiser (f2: the scales written straight
+// into the layout the tensor core reads). Rows are cut into tiles of
+// `tile_rows` rows, tokens into 128-token steps on the global grid; block h of
+// tile t at step g holds tile rows 128 h .. 128 h + 127, and its 512 bytes
+// hold row r, 32-token block kb at byte (r % 32) * 16 + (r / 32) * 4 + kb.
+// Rows past R and tokens past M are zero.
+struct SfOut {
+    uint8_t* sf;       // nullptr: no block output
+    int tile_rows;     // rows per tile
+    int nblk;          // 128-row blocks per tile: ceil(tile_rows / 128)
+    long long steps;   // 128-token grid steps: ceil(M / 128)
+    int rows_out;      // rows covered by the blocks: tiles * tile_rows
+    int tiles;         // ceil(R / tile_rows)
+    int dead;          // rows of a tile's last block past the tile: nblk * 128 - tile_rows
+};
+
+__device__ __forceinline__ void sf_store(const SfOut& o, int f, long long step, int kb, uint8_t v) {
+    const int t = f / o.tile_rows;
+    const int rt = f - t * o.tile_rows;
+    const int h = rt >> 7, r = rt & 127;
+    const size_t atom = (static_cast<size_t>(t) * o.steps + step) * o.nblk + h;
+    o.sf[atom * 512 + (r & 31) * 16 + (r >> 5) * 4 + kb] = v;
+}
+
 __global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(const uint16_t* __restrict__ x,
                                                                              long long M, int R, int vec,
                                                                              uint8_t* __restrict__ q,
-                                                                             uint8_t* __restrict__ s) {
+                                                                             uint8_t* __restrict__ s,
+                                                                             const SfOut sfo) {
     extern __shared__ __align__(16) uint4 sT[];  // [QX_FEAT][16] pieces of 8 bf16 (tokens)
     const long long t0 = static_cast<long long>(blockIdx.x) * QX_TOK;
     const int f0 = blockIdx.y * QX_FEAT;
@@ -150,12 +175,38 @@ __global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(con
     __syncthreads();
     const int b = lane >> 3;                    // 32-token block of the tile
     const long long tb = t0 + 32 * b;           // its first token
-    if (tb >= M) return;                        // M % 32 == 0: a block is all in or all out
+    const long long step = t0 / QX_TOK;         // this block's 128-token grid step
+    if (sfo.sf && sfo.dead > 0 && blockIdx.y == 0) {
+        // rows of each tile's last 128-row block that lie past the tile map to
+        // no feature: zero their four scale bytes (one aligned word per row)
+        const int live = sfo.tile_rows - 128 * (sfo.nblk - 1);
+        for (int i = threadIdx.x; i < sfo.tiles * sfo.dead; i += QX_THREADS) {
+            const int t = i / sfo.dead;
+            const int r = live + (i - t * sfo.dead);
+            const size_t atom = (static_cast<size_t>(t) * sfo.steps + step) * sfo.nblk + (sfo.nblk - 1);
+            *reinterpret_cast<uint32_t*>(sfo.sf + atom * 512 + (r & 31) * 16 + (r >> 5) * 4) = 0u;
+        }
+    }
+    if (tb >= M || f0 >= R) {
+        // tokens past M (M % 32 == 0: a block is all in or all out) or rows
+        // past R: only zero scale-factor bytes to write
+        if (sfo.sf) {
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                const int f = f0 + 16 * warp + 8 * pass + (lane & 7);
+                if (f < sfo.rows_out) sf_store(sfo, f, step, b, 0);
+            }
+        }
+        return;
+    }
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         const int fl = 16 * warp + 8 * pass + (lane & 7);
         const int f = f0 + fl;
-        if (f >= R) continue;
+        if (f >= R) {
+            if (sfo.sf && f < sfo.rows_out) sf_store(sfo, f, step, b, 0);
+            continue;
+        }
         float v[32];
         uint32_t amax_bits = 0;
 #pragma unroll
@@ -171,7 +222,7 @@ __global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(con
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax_bits = max(amax_bits, __float_as_uint(v[i]) & 0x7fffffffu);
         uint8_t* qdst = q + static_cast<long long>(f) * M + tb;
-        uint8_t* sdst = s + static_cast<long long>(f) * (M / 32) + (tb >> 5);
+        uint8_t* sdst = s ? s + static_cast<long long>(f) * (M / 32) + (tb >> 5) : nullptr;
         uint32_t w[8];
         uint8_t sbyte;
         if (amax_bits >= 0x7f800000u) {  // NaN or Inf in the block
@@ -199,21 +250,38 @@ __global__ void __launch_bounds__(QX_THREADS) quantize_transpose_bf16_kernel(con
             reinterpret_cast<uint4*>(qdst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
             reinterpret_cast<uint4*>(qdst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-        *sdst = sbyte;
+        if (s) *sdst = sbyte;
+        if (sfo.sf) sf_store(sfo, f, step, b, sbyte);
     }
 }
 
 cudaError_t launch_quantize_transpose(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s,
                                       cudaStream_t stream) {
+    return launch_quantize_transpose_sf(x, M, R, q, s, nullptr, 0, stream);
+}
+
+cudaError_t launch_quantize_transpose_sf(const uint16_t* x, int64_t M, int R, uint8_t* q, uint8_t* s, uint8_t* sf,
+                                         int tile_rows, cudaStream_t stream) {
+    SfOut sfo;
+    sfo.sf = sf;
+    sfo.tile_rows = tile_rows > 0 ? tile_rows : 128;
+    sfo.nblk = (sfo.tile_rows + 127) / 128;
+    sfo.steps = (M + QX_TOK - 1) / QX_TOK;
+    const long long tiles = (R + sfo.tile_rows - 1) / sfo.tile_rows;
+    sfo.rows_out = static_cast<int>(tiles * sfo.tile_rows);
+    sfo.tiles = static_cast<int>(tiles);
+    sfo.dead = sfo.nblk * 128 - sfo.tile_rows;
     // bit 0: 16-byte loads of x rows; bit 1: 32-byte stores of q (M % 32 == 0 keeps every block aligned)
     const int vec = (((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (R % 8) == 0) ? 1 : 0) |
                     ((reinterpret_cast<uintptr_t>(q) & 31u) == 0 ? 2 : 0);
     const long long gx = (M + QX_TOK - 1) / QX_TOK;
-    const int gy = (R + QX_FEAT - 1) / QX_FEAT;
+    // with block output, the blocks past R cover the last tile's padding rows
+    const int rows = sf ? (sfo.rows_out > R ? sfo.rows_out : R) : R;
+    const int gy = (rows + QX_FEAT - 1) / QX_FEAT;
     if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
     constexpr size_t smem = sizeof(uint16_t) * QX_FEAT * QX_TOK;  // 32 KB
     quantize_transpose_bf16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), QX_THREADS, smem,
-                                     stream>>>(x, M, R, vec, q, s);
+                                     stream>>>(x, M, R, vec, q, s, sfo);
     return cudaGetLastError();
 }
 

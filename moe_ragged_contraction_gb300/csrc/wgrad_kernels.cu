@@ -48,6 +48,12 @@
 #ifndef MXW_COLLECTOR_A
 #define MXW_COLLECTOR_A 1
 #endif
+// The producers of the persistent grid meet at the passes that follow a pass
+// spanning two experts (pass_barrier_at): 1 always, 0 never, -1 where
+// use_pass_barrier() predicts a gain.
+#ifndef MXW_PASS_BARRIER
+#define MXW_PASS_BARRIER -1
+#endif
 // Order of an expert's tiles: -1 the side with fewer rows fastest, 0 the N
 // side's tiles fastest, 1 the M side's.
 #ifndef MXW_ORDER
@@ -120,7 +126,7 @@ __device__ __forceinline__ uint32_t load_scale4_edge(const uint8_t* __restrict__
 // first, then the N side's.
 __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs, const PrepSide sm_side,
                                                            const PrepSide sn_side, int32_t* __restrict__ plan, int E,
-                                                           long long M, int ts_max) {
+                                                           long long M, int ts_max, int grid) {
     extern __shared__ int prep_smem[];
     int* s_start = prep_smem;        // [E]
     int* s_end = s_start + E;        // [E]: raw offs first, then the clamped ends
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         if (threadIdx.x == 0) {
             plan[0] = TS;
             plan[1] = E;
+            plan[2] = 0;  // the main kernel's pass-barrier counter
             if (s_flags) atomicOr(&g_device_status, s_flags);
         }
         int32_t* ex = plan + PLAN_HDR;
@@ -200,8 +207,15 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
             const int len = s_end[g] - s_start[g];
             ex[4 * g + 0] = s_start[g];
             ex[4 * g + 1] = len;
-            ex[4 * g + 2] = (len + BK - 1) / BK;
-            ex[4 * g + 3] = s_sb[g];
+            if (grid) {
+                // K-steps on the global 128-token grid: the steps the run
+                // touches, and the grid step of its first token
+                ex[4 * g + 2] = len ? (s_start[g] + len + BK - 1) / BK - s_start[g] / BK : 0;
+                ex[4 * g + 3] = s_start[g] / BK;
+            } else {
+                ex[4 * g + 2] = (len + BK - 1) / BK;
+                ex[4 * g + 3] = s_sb[g];
+            }
             int rank = 0;  // longest first; equal lengths keep expert order
             for (int h = 0; h < E; ++h) {
                 const int lh = s_end[h] - s_start[h];
@@ -565,6 +579,9 @@ struct MainParams {
     int nblk_n;              // 128-row scale blocks per N-side tile
     int kn;                  // 0: M side = rows of A (n), N side = rows of B (k); 1: swapped
     int m_fastest;           // mode 0: an expert's tiles ordered M-side tile fastest (else N-side tile fastest)
+    int grid;                // mode 0: K-steps on the global 128-token grid (scale blocks per grid step)
+    int pass_bar;            // mode 0: producers meet at the passes that follow one spanning two experts
+    unsigned int* pass_ctr;  // their arrival counter (zeroed by the prep kernel)
     int stages, sf_slots;
     int acc_bufs;            // accumulators in TMEM (2: the next tile's MMAs overlap this tile's drain)
     int wide_stores;         // 32-byte output stores (rows of 16 columns 32-byte aligned), else 16-byte
@@ -612,6 +629,7 @@ struct Item {
     int g, tm, tn;        // expert, M-side and N-side tile
     int start, len;       // contraction: first coordinate and length
     int nsteps;           // K-steps
+    int kk0;              // 32-token chunks of the first K-step before the run's first token (grid K-steps)
     int m0, m_end;        // M-side rows of the tile start at m0; rows at or past m_end are not stored
     int sfm, sfn;         // scale-factor block rows of the tile's first K-step (M side: this CTA adds its rank)
     int z;                // N-side tensor-map depth coordinate (the expert in the grouped GEMM)
@@ -639,8 +657,14 @@ __device__ __forceinline__ Item load_item(const MainParams& p, long long i) {
             it.tm = t / p.tiles_n;
             it.tn = t - it.tm * p.tiles_n;
         }
-        it.start = __ldg(ex + 4 * it.g + 0);
-        it.len = __ldg(ex + 4 * it.g + 1);
+        const int start = __ldg(ex + 4 * it.g + 0);
+        const int len = __ldg(ex + 4 * it.g + 1);
+        // grid K-steps start at the run's 128-token grid step; its leading
+        // chunks belong to the run before and are skipped
+        const int lead = p.grid ? (start & (BK - 1)) : 0;
+        it.start = start - lead;
+        it.len = len + lead;
+        it.kk0 = lead >> 5;
         it.nsteps = __ldg(ex + 4 * it.g + 2);
         const int sb = __ldg(ex + 4 * it.g + 3);
         it.m0 = it.tm * (2 * BM);
@@ -659,6 +683,7 @@ __device__ __forceinline__ Item load_item(const MainParams& p, long long i) {
         it.m_end = e.z;
         it.start = 0;
         it.len = p.K;
+        it.kk0 = 0;
         it.nsteps = p.ksteps;
         it.sfm = mt * p.ksteps * 2;
         it.sfn = (it.g * p.tiles_n + it.tn) * p.ksteps * p.nblk_n;
@@ -687,16 +712,44 @@ __device__ __forceinline__ long long next_item(long long& pass, int G, int pair,
     return -1;
 }
 
+// Whether the producers meet before pass q of the static schedule (q >= 1):
+// pass q is full (every pair has an item in it) and pass q - 1 spans an
+// expert boundary (items of two experts, possibly of different lengths).
+__device__ __forceinline__ bool pass_barrier_at(long long q, int G, long long total, int ntpe) {
+    if (q < 1 || (q + 1) * G > total) return false;
+    return ((q - 1) * G) / ntpe != (q * G - 1) / ntpe;
+}
+
+// Grid barrier among the producers (one lane per CTA): arrive, then wait
+// until `target` arrivals; bounded like every other wait here.
+__device__ __forceinline__ bool pass_barrier_wait(unsigned int* ctr, unsigned int target, volatile int* abort_flag,
+                                                  unsigned long long wait_ns) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > wait_ns) {
+            *abort_flag = 1;
+            atomicOr(&g_device_status, MXFP8_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+
 // This pair's items in schedule order, the next item's plan entry loaded one
 // item ahead so that its global-memory latency overlaps the current item.
 struct ItemStream {
     const MainParams& p;
     int G, pair;
-    long long total, pass, i_next;
+    long long total, pass, i_next, cur;  // cur: index of the item next() returned last
     Item it_next;
 
     __device__ __forceinline__ ItemStream(const MainParams& p_, int G_, int pair_, long long total_)
-        : p(p_), G(G_), pair(pair_), total(total_), pass(0) {
+        : p(p_), G(G_), pair(pair_), total(total_), pass(0), cur(-1) {
         i_next = next_item(pass, G, pair, total);
         if (i_next >= 0) it_next = load_item(p, i_next);
     }
@@ -704,6 +757,7 @@ struct ItemStream {
     __device__ __forceinline__ bool next(Item& it) {
         if (i_next < 0) return false;
         it = it_next;
+        cur = i_next;
         i_next = next_item(pass, G, pair, total);
         if (i_next >= 0) it_next = load_item(p, i_next);
         return true;
@@ -782,7 +836,7 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
             const uint32_t a_s = a_s0 + stg * A_STAGE;
             const uint32_t b_s = b_s0 + stg * b_stage;
             const uint32_t sel = (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
-            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t acc = (s > 0 || kk > it.kk0) ? 1u : 0u;
             const uint64_t ad = desc_kmajor_sw128(a_s + 32 * kk);
             if (TWO && MXW_COLLECTOR_A) {
                 // both MMAs of the chunk multiply the same A tile: the
@@ -805,7 +859,7 @@ __device__ __forceinline__ void mma_issue(const MainParams& p, const MmaCtx& x) 
                 copy_sf(st, slot);
                 const int rem = it.len - s * BK;
                 const int nk = rem >= BK ? 4 : (rem >> 5);
-                for (int kk = 0; kk < nk; ++kk) mma_chunk(s, kk, st, slot);
+                for (int kk = s == 0 ? it.kk0 : 0; kk < nk; ++kk) mma_chunk(s, kk, st, slot);
                 tc_commit_pair_elect(x.bar_empty + 8 * st, 0x3);  // frees the stage in both CTAs
             }
             named_bar_arrive(BAR_FREE + st, 64);
@@ -900,7 +954,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAIN_THREADS, 1)
             bool ok = true;
             ItemStream items(p, G, pair, total);
             Item it;
+            unsigned int nbar = 0;  // pass barriers met so far
             while (ok && items.next(it)) {
+                if (p.pass_bar && pass_barrier_at(items.cur / G, G, total, nt_per_expert)) {
+                    // Pass q starts together on every pair after a pass that held
+                    // two experts' tiles (of different lengths): pairs that share
+                    // an expert's operands then stream them at the same time and
+                    // meet in L2 instead of re-reading them from DRAM. Every CTA
+                    // of the grid is resident (the grid is the resident pairs),
+                    // every CTA has exactly one item in a full pass, and the wait
+                    // is bounded (an abort elsewhere ends it as a timeout here).
+                    ++nbar;
+                    ok = pass_barrier_wait(p.pass_ctr, nbar * gridDim.x, abort_flag, p.wait_ns);
+                    if (!ok) break;
+                }
                 const int m_row = it.m0 + static_cast<int>(rank) * BM;
                 const int n_row1 = it.tn * p.tn + static_cast<int>(rank) * h1;
                 const int n_row2 = it.tn * p.tn + p.n1 + static_cast<int>(rank) * h2;
@@ -1390,6 +1457,26 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, b
     return best;
 }
 
+// Whether the weight gradient's producers should meet at expert boundaries
+// (pass_barrier_at). A pass of the G pairs covers G consecutive tiles; the
+// operand indexed by the faster-moving tile index is shared by the pairs
+// `inner` apart in a pass (G / inner of them), and pairs that start their
+// tiles at different times stream it at different times, so the L2 no longer
+// serves them all and it is re-read from DRAM (measured at 671B down:
+// 11-18 GB read per launch against 5 GB of operands, 7.2 GB with the
+// barrier). The barrier costs the idle time of the pairs that finish a pass
+// early, small only when a pass mostly holds one expert. Measured on GB300
+// with one call per variant: 671B down (140 tiles per expert, 15 pairs
+// sharing each N-side tile) +2.6% back to back; 671B up/gate (256 tiles, 4.75
+// pairs sharing each M-side stripe) -1%; 16B and 16B production (32 tiles
+// per expert, two or three experts per pass) -6% and -2.5%. On: at least one
+// pass of tiles per expert and at least 8 pairs sharing each far tile.
+int use_pass_barrier(const TileConfig& tc, int G) {
+    const long long ntpe = static_cast<long long>(tc.tiles_m) * tc.tiles_n;
+    const int inner = tc.m_fastest ? tc.tiles_m : tc.tiles_n;
+    return (ntpe >= G && G >= 8 * inner) ? 1 : 0;
+}
+
 static cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& geo, long long items,
                                const CUtensorMap* maps, int dev, int num_sms, cudaStream_t stream,
                                cudaEvent_t ev_before, cudaEvent_t ev_after);
@@ -1472,9 +1559,14 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         sn_side.tiles = tc.tiles_n;
         sn_side.blocks = tc.nblk_n;
         sn_side.sf = a.ws + L.sfn_off;
+        if (a.grid) {
+            // the caller's scale-factor blocks: the prep only writes the plan
+            sm_side.rows = sn_side.rows = 0;
+            sm_side.tiles = sn_side.tiles = 0;
+        }
         // enough blocks for every task of the largest possible plan, at most as
         // many as are resident at once (one wave)
-        const long long tasks = (2LL * tc.tiles_m + static_cast<long long>(tc.nblk_n) * tc.tiles_n) *
+        const long long tasks = (2LL * sm_side.tiles + static_cast<long long>(tc.nblk_n) * sn_side.tiles) *
                                 ((L.ts_max + PREP_TILE_STEPS - 1) / PREP_TILE_STEPS);
         const size_t sm = sizeof(int) * (3 * static_cast<size_t>(a.E) + 1) +
                           sizeof(uint32_t) * PREP_ROWS * (PREP_TILE_STEPS + 1);
@@ -1496,7 +1588,7 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         if (blocks > static_cast<long long>(per_sm) * a.num_sms) blocks = static_cast<long long>(per_sm) * a.num_sms;
         if (blocks < 1) blocks = 1;
         wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(a.offs, sm_side, sn_side, plan, a.E,
-                                                                                    a.M, L.ts_max);
+                                                                                    a.M, L.ts_max, a.grid);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -1506,6 +1598,8 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
     mp.plan = plan;
     mp.out = a.out;
     mp.mode = 0;
+    mp.grid = a.grid;
+    mp.pass_ctr = reinterpret_cast<unsigned int*>(plan + 2);  // (pass_bar: set in launch_main)
     mp.out_stride = a.K;
     mp.col_limit = a.K;
     mp.ksteps = 0;
@@ -1570,6 +1664,7 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     mp.tma_store = (mp.tma_store && geo.stg_bufs > 0 && (!tc.kn || mp.mode == 0)) ? 1 : 0;
     mp.b_stage = geo.b_stage;
     const int pairs = static_cast<int>(items < mp_dev ? (items > 0 ? items : 1) : mp_dev);
+    if (mp.mode == 0) mp.pass_bar = MXW_PASS_BARRIER >= 0 ? MXW_PASS_BARRIER : use_pass_barrier(tc, pairs);
     if (ev_before) {
         cudaError_t e = cudaEventRecord(ev_before, stream);
         if (e != cudaSuccess) return e;
@@ -1582,11 +1677,15 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     cfg.blockDim = dim3(MAIN_THREADS);
     cfg.dynamicSmemBytes = geo.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // the pass barrier has CTAs wait on one another: a cooperative launch
+    // guarantees that every CTA of the grid is resident at once
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = mp.pass_bar ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], mp);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
@@ -1738,6 +1837,9 @@ cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap* maps, const char**
     mp.N = a.N;
     mp.K = a.K;
     mp.ts_max = 0;
+    mp.grid = 0;
+    mp.pass_bar = 0;
+    mp.pass_ctr = nullptr;
     mp.tiles_m = 0;
     mp.tma_store = a.tma_store;
     mp.wide_stores = (tc.tn % 32 == 0 && a.N % 16 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) ? 1 : 0;

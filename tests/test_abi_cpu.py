@@ -253,3 +253,39 @@ def test_epilogue_store_setting(lib):
                 mx.set_epilogue_store(bad)
     finally:
         mx.set_epilogue_store(0)
+
+
+def test_sf_blocks_bytes(lib):
+    """Size of the scale-factor blocks: tiles x 128-token grid steps x
+    128-row blocks per tile x 512 bytes; 0 for sizes the layout rejects."""
+    f = lib.mxfp8_sf_blocks_bytes
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int]
+    f.restype = ctypes.c_size_t
+    assert f(2048, 32768, 256) == 8 * 256 * 2 * 512
+    assert f(1408, 32768, 352) == 4 * 256 * 3 * 512
+    assert f(7168, 524288, 416) == 18 * 4096 * 4 * 512
+    assert f(100, 96, 16) == 7 * 1 * 1 * 512          # partial tile, partial step
+    assert f(0, 1024, 256) == 0 and f(64, 1000, 256) == 0 and f(64, 1024, 17) == 0 and f(64, 1024, 0) == 0
+
+
+def test_sf_entry_points_validation(lib):
+    """Argument checks of the scale-factor-block path, taken on the host before
+    any device call."""
+    w = lib.mxfp8_wgrad_grouped_sf
+    w.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    ok = (P, P, P, P, P)
+    assert w(*ok, 4, 128, 256, 1024, 2, 256, P, None) == _lib.EINVAL      # kn not 0 or 1
+    assert w(*ok, 4, 128, 256, 1024, 0, 17, P, None) == _lib.EINVAL       # tn not a multiple of 16
+    assert w(*ok, 4, 128, 256, 1024, 0, 464, P, None) == _lib.EINVAL      # tn above 448
+    assert w(P, P + 4, P, P, P, 4, 128, 256, 1024, 0, 256, P, None) == _lib.EALIGN  # sfA not 16-byte aligned
+    assert w(P, None, P, P, P, 4, 128, 256, 1024, 0, 256, P, None) == _lib.EINVAL   # null sfA
+    assert w(*ok, 4, 128, 256, 1000, 0, 256, P, None) == _lib.EINVAL     # M % 32 != 0
+    assert w(None, None, None, None, None, 0, 128, 256, 1024, 0, 256, None, None) == _lib.OK  # E = 0: no-op
+    q = lib.mxfp8_quantize_transpose_bf16_sf
+    q.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 4
+    assert q(P, 1024, 64, 0, P, None, P, None) == _lib.EINVAL     # tile_rows < 16
+    assert q(P, 1024, 64, 24, P, None, P, None) == _lib.EINVAL    # tile_rows % 16 != 0
+    assert q(P, 1024, 64, 256, P, None, None, None) == _lib.EINVAL  # null sf
+    assert q(P, 1000, 64, 256, P, None, P, None) == _lib.EINVAL   # M % 32 != 0
+    assert q(P, 1024, 64, 256, P + 8, None, P, None) == _lib.EALIGN  # q not 16-byte aligned
