@@ -13,6 +13,17 @@
 #include "mxw_internal.h"
 #include "../../include/mxfp8_wgrad.h"
 
+// 1: the regular entry points also run each expert's K-steps on the global
+// 128-token grid: the prep's scale gather then does not depend on the routing
+// (it starts at the kernel's entry, only the plan waits for offs) and the
+// operand tiles start on 128-byte boundaries. Measured on GB300 against
+// K-steps that start at each run's first token (same output bits),
+// back-to-back throughput in one call: 671B down +1.4%, 671B up/gate +2.4%,
+// 16B +1.9%, 16B production +2.2%.
+#ifndef MXW_GRID_KSTEPS
+#define MXW_GRID_KSTEPS 1
+#endif
+
 namespace {
 
 thread_local char g_err[512] = "no error";
@@ -366,7 +377,8 @@ int run(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB
     a.ev_before = evb;
     a.ev_after = eva;
     a.stall_first_stage = stall;
-    a.grid = sfu ? 1 : 0;
+    a.grid = sfu ? 1 : MXW_GRID_KSTEPS;
+    a.gather = sfu ? 0 : 1;
     // output as [E][N][K] for the TMA-store epilogue (used where its staging fits)
     a.tma_store = (store_mode() == 0 && make_out_map(&maps[5], out, K, N, E)) ? 1 : 0;
     if (!a.tma_store) maps[5] = maps[0];

@@ -75,8 +75,10 @@ struct WgradArgs {
     cudaEvent_t ev_before, ev_after;
     int stall_first_stage;  // failure-path test hook (0 in normal use)
     int tma_store;          // maps[5] describes out: TMA-store epilogue where its staging fits
-    int grid;               // 1: K-steps on the global 128-token grid, scale blocks given by the
-                            // caller (maps[3], maps[4]; lay.ts_max = grid steps); the prep writes the plan only
+    int grid;               // 1: K-steps on the global 128-token grid (scale blocks per grid step)
+    int gather;             // 1: the prep kernel lays the scale planes out into the workspace;
+                            // 0: maps[3], maps[4] describe the caller's blocks (grid == 1,
+                            // lay.ts_max = grid steps) and the prep writes the plan only
 };
 
 // Enqueue the plan / scale re-layout kernel and the main contraction kernel.

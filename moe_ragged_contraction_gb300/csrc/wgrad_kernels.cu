@@ -145,54 +145,61 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     // Every block of this grid is resident once all have passed here, so the
     // main kernel's CTAs only queue behind them for shared memory.
     griddep_launch_dependents();
-    for (int g = threadIdx.x; g < E; g += PREP_THREADS) s_end[g] = offs[g];
-    __syncthreads();
-    if (warp == 0) {
-        int carry_end = 0, carry_steps = 0, flags = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int g = base + lane;
-            int o = 0;
-            if (g < E) {
-                o = s_end[g];
-                if (o < 0) { o = 0; flags |= MXFP8_DEV_OFFS_RANGE; }
-                if (o > Mi) { o = Mi; flags |= MXFP8_DEV_OFFS_RANGE; }
-                if (o & 31) { o &= ~31; flags |= MXFP8_DEV_OFFS_ALIGN; }
+    // On the global 128-token grid (grid != 0) the scale blocks do not depend
+    // on the routing: only block 0 (the plan) reads offs, the others go
+    // straight to the gather.
+    const bool need_scan = !grid || blockIdx.x == 0;
+    if (need_scan) {
+        for (int g = threadIdx.x; g < E; g += PREP_THREADS) s_end[g] = offs[g];
+        __syncthreads();
+        if (warp == 0) {
+            int carry_end = 0, carry_steps = 0, flags = 0;
+            for (int base = 0; base < E; base += 32) {
+                const int g = base + lane;
+                int o = 0;
+                if (g < E) {
+                    o = s_end[g];
+                    if (o < 0) { o = 0; flags |= MXFP8_DEV_OFFS_RANGE; }
+                    if (o > Mi) { o = Mi; flags |= MXFP8_DEV_OFFS_RANGE; }
+                    if (o & 31) { o &= ~31; flags |= MXFP8_DEV_OFFS_ALIGN; }
+                }
+                int m = o;  // inclusive running max -> clamped non-decreasing ends
+    #pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    int t = __shfl_up_sync(full, m, d);
+                    if (lane >= d) m = max(m, t);
+                }
+                const int end = max(m, carry_end);
+                int start = __shfl_up_sync(full, end, 1);
+                if (lane == 0) start = carry_end;
+                if (g < E && o < start) flags |= MXFP8_DEV_OFFS_UNSORTED;
+                const int ns = (end - start + BK - 1) / BK;
+                int incl = ns;
+    #pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    int t = __shfl_up_sync(full, incl, d);
+                    if (lane >= d) incl += t;
+                }
+                __syncwarp();
+                if (g < E) {
+                    s_start[g] = start;
+                    s_end[g] = end;
+                    s_sb[g] = carry_steps + incl - ns;
+                }
+                carry_end = __shfl_sync(full, end, 31);
+                carry_steps += __shfl_sync(full, incl, 31);
             }
-            int m = o;  // inclusive running max -> clamped non-decreasing ends
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                int t = __shfl_up_sync(full, m, d);
-                if (lane >= d) m = max(m, t);
+    #pragma unroll
+            for (int d = 16; d > 0; d >>= 1) flags |= __shfl_xor_sync(full, flags, d);
+            if (lane == 0) {
+                s_sb[E] = carry_steps;
+                s_flags = flags;
             }
-            const int end = max(m, carry_end);
-            int start = __shfl_up_sync(full, end, 1);
-            if (lane == 0) start = carry_end;
-            if (g < E && o < start) flags |= MXFP8_DEV_OFFS_UNSORTED;
-            const int ns = (end - start + BK - 1) / BK;
-            int incl = ns;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                int t = __shfl_up_sync(full, incl, d);
-                if (lane >= d) incl += t;
-            }
-            __syncwarp();
-            if (g < E) {
-                s_start[g] = start;
-                s_end[g] = end;
-                s_sb[g] = carry_steps + incl - ns;
-            }
-            carry_end = __shfl_sync(full, end, 31);
-            carry_steps += __shfl_sync(full, incl, 31);
         }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) flags |= __shfl_xor_sync(full, flags, d);
-        if (lane == 0) {
-            s_sb[E] = carry_steps;
-            s_flags = flags;
-        }
+        __syncthreads();
     }
-    __syncthreads();
-    const int TS = s_sb[E];
+    // K-steps the blocks cover: every expert's own steps, or the grid's
+    const int TS = grid ? static_cast<int>((M + BK - 1) / BK) : s_sb[E];
 
     if (blockIdx.x == 0) {
         if (threadIdx.x == 0) {
@@ -255,7 +262,12 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         const int gs = gs0 + lane;
         long long col = 0;
         int nvalid = 0;
-        if (gs < TS) {
+        if (gs < TS && grid) {
+            // grid step gs: 32-token blocks 4 gs .. 4 gs + 3 of every row
+            col = 4LL * gs;
+            const long long left = M / 32 - col;
+            nvalid = static_cast<int>(left < 4 ? left : 4);
+        } else if (gs < TS) {
             int lo = 0, hi = E;  // expert owning gs: the last g with s_sb[g] <= gs
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
@@ -1559,7 +1571,7 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         sn_side.tiles = tc.tiles_n;
         sn_side.blocks = tc.nblk_n;
         sn_side.sf = a.ws + L.sfn_off;
-        if (a.grid) {
+        if (!a.gather) {
             // the caller's scale-factor blocks: the prep only writes the plan
             sm_side.rows = sn_side.rows = 0;
             sm_side.tiles = sn_side.tiles = 0;
