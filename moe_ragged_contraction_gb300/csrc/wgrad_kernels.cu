@@ -126,7 +126,7 @@ __device__ __forceinline__ uint32_t load_scale4_edge(const uint8_t* __restrict__
 // first, then the N side's.
 __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs, const PrepSide sm_side,
                                                            const PrepSide sn_side, int32_t* __restrict__ plan, int E,
-                                                           long long M, int ts_max, int grid) {
+                                                           long long M, int ts_max, int grid, int prefetch) {
     extern __shared__ int prep_smem[];
     int* s_start = prep_smem;        // [E]
     int* s_end = s_start + E;        // [E]: raw offs first, then the clamped ends
@@ -137,8 +137,10 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     const unsigned full = 0xffffffffu;
     const int Mi = static_cast<int>(M);
 
-    prefetch_share_l2(sm_side.plane, static_cast<size_t>(sm_side.rows) * static_cast<size_t>(M / 32));
-    prefetch_share_l2(sn_side.plane, static_cast<size_t>(sn_side.rows) * static_cast<size_t>(M / 32));
+    if (prefetch) {
+        prefetch_share_l2(sm_side.plane, static_cast<size_t>(sm_side.rows) * static_cast<size_t>(M / 32));
+        prefetch_share_l2(sn_side.plane, static_cast<size_t>(sn_side.rows) * static_cast<size_t>(M / 32));
+    }
     // the main kernel may launch now: its prologue (barriers, TMEM, tensor
     // maps) overlaps this kernel, and it waits for this grid's completion (and
     // the visibility of its writes) before it reads the plan or the scales.
@@ -1599,8 +1601,16 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         long long blocks = tasks;
         if (blocks > static_cast<long long>(per_sm) * a.num_sms) blocks = static_cast<long long>(per_sm) * a.num_sms;
         if (blocks < 1) blocks = 1;
+        // The L2 prefetch of the planes at the prep's entry pays while its
+        // gather waits for offs, or while the planes fit well within L2 (16B:
+        // the flushed step 2% faster with it); on the grid with planes of
+        // 90-150 MB (the 671B shapes) the prefetched lines are evicted before
+        // the gather reaches them (671B down: 236 MB read instead of 151,
+        // 72 instead of 62 us).
+        const size_t plane_bytes = (static_cast<size_t>(sm_side.rows) + sn_side.rows) * static_cast<size_t>(a.M / 32);
+        const int prefetch = (!a.grid || plane_bytes <= (size_t(64) << 20)) ? 1 : 0;
         wgrad_prep<<<static_cast<unsigned>(blocks), PREP_THREADS, sm, a.stream>>>(a.offs, sm_side, sn_side, plan, a.E,
-                                                                                    a.M, L.ts_max, a.grid);
+                                                                                    a.M, L.ts_max, a.grid, prefetch);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
