@@ -221,7 +221,9 @@ int mxfp8_quantize_transpose_bf16_sf(const uint16_t* x, int64_t M, int R, int ti
  * rows on B, kn = 1 the reverse (mxfp8_wgrad_tile_config reports the
  * library's choice); sfA holds A's scales as SF blocks for tiles of
  * (kn ? tn : 256) rows and sfB B's for tiles of (kn ? 256 : tn) rows, both
- * 16-byte aligned. tn is a multiple of 16 in [16, 448] (MXFP8_EINVAL
+ * 16-byte aligned and at least mxfp8_sf_blocks_bytes(N, M, kn ? tn : 256)
+ * and mxfp8_sf_blocks_bytes(K, M, kn ? 256 : tn) bytes long (the kernels
+ * read that much; the host cannot check the allocations' sizes). tn is a multiple of 16 in [16, 448] (MXFP8_EINVAL
  * otherwise). Each expert's K-steps run on the 128-token grid: a run that
  * starts inside a step skips that step's leading 32-token chunks, so every
  * output element sums the same 32-token block products in the same order as

@@ -286,7 +286,22 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
         // rows of the plane this block may read: inside its tile and the plane
         const int rows_lim = min(rows, row0 - in_tile0 + tile_rows);
         uint32_t wv[ROWS_PER_WARP];
-        if (nvalid > 0 && static_cast<size_t>(rows_lim - 1) * sM + col + 8 <= plane_bytes) {
+        // on the grid with 4-byte-aligned rows every step's 4 scale bytes are
+        // one aligned word: one load per row
+        const bool words = grid && ((reinterpret_cast<uintptr_t>(plane) | static_cast<uintptr_t>(sM)) & 3) == 0;
+        if (words && nvalid > 0 && static_cast<size_t>(rows_lim - 1) * sM + col + 4 <= plane_bytes) {
+            uint32_t v[ROWS_PER_WARP];
+#pragma unroll
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int row = min(row0 + warp + i * (PREP_THREADS / 32), rows_lim - 1);
+                v[i] = __ldg(reinterpret_cast<const uint32_t*>(plane + static_cast<size_t>(row) * sM + col));
+            }
+#pragma unroll
+            for (int i = 0; i < ROWS_PER_WARP; ++i) {
+                const int row = row0 + warp + i * (PREP_THREADS / 32);
+                wv[i] = row < rows_lim ? (v[i] & keep) : 0u;
+            }
+        } else if (nvalid > 0 && static_cast<size_t>(rows_lim - 1) * sM + col + 8 <= plane_bytes) {
             // every word this lane reads lies inside the plane: rows past the
             // limit read the last valid row and are zeroed afterwards
             // all loads first, then the shifts: the words of every row in flight together
@@ -1709,6 +1724,14 @@ cudaError_t launch_main(MainParams& mp, const TileConfig& tc, const Geometry& ge
     cfg.attrs = attr;
     cfg.numAttrs = mp.pass_bar ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], mp);
+    if (e != cudaSuccess && mp.pass_bar) {
+        // the grid could not be made co-resident (another context holds SMs):
+        // run without the barrier, which needs no co-residency
+        (void)cudaGetLastError();
+        mp.pass_bar = 0;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, wgrad_main, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], mp);
+    }
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
