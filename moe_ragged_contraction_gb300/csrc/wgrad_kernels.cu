@@ -1452,10 +1452,14 @@ TileConfig make_config(int kn, int tn, int rows_m, int rows_n) {
 // the transposed 4-byte stores of the 256 side on B), 205 a fixed per-tile
 // cost; widths whose TMA-store staging fits and whose chunks are all staged
 // (tn % 64 == 0) have the floor 3.7 tn + 815 instead. The 256 side on B also
-// measured about 8% slower on long tiles with its 4-byte register stores and
-// about 4% slower where its chunks go through TMA stores (the 16B and 671B
-// down expert shapes: tn = 352 and 448 against 416 on A, weighed with the
-// column costs above).
+// measured, weighed with the column costs above, about 8% slower on long
+// tiles with its 4-byte register stores; about 4% slower where its chunks go
+// through TMA stores but half a chunk still leaves from registers (tn % 64 ==
+// 32: 8 x 4 tiles of 352 on B against 6 x 5 of 416 on A at the 16B expert
+// shape; 28 x 10 tiles of 416 on B ran 8% slower than 16 x 16 of 448 on A at
+// the 671B up/gate shape); and about 1% faster where every chunk is staged
+// (tn % 64 == 0: 16 x 8 tiles of 448 on B ran 1.8% faster than 28 x 5 of 416
+// on A at the 671B down shape, main kernel, four interleaved pairs of runs).
 TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, bool wide_ok, double* cost) {
     TileConfig best{};
     double best_cost = -1.0;
@@ -1466,7 +1470,7 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, b
         const TileConfig tc = make_config(kn, tn, rows_m, rows_n);
         const bool wide = !kn && wide_ok && tn % 32 == 0;
         const double w_floor = kn ? 17.0 : (wide ? 6.6 : 13.0);
-        const double kn_factor = g.stg_bufs > 0 ? 1.04 : 1.08;
+        const double kn_factor = g.stg_bufs == 0 ? 1.08 : (tn % 64 == 0 ? 0.99 : 1.04);
         const double run = (steps + (g.acc_bufs == 1 && tn > 256 ? 3.0 : 0.0)) * tn * column_cost(tn) * (kn ? kn_factor : 1.0);
         double per_tile = (run > w_floor * tn ? run : w_floor * tn) + 205.0;
         if (!kn && g.stg_bufs > 0 && tn % 64 == 0) {

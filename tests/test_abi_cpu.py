@@ -114,8 +114,12 @@ def test_tile_config_choice(lib):
         assert mx.tile_config(8, 1408, 2048, 196608) == {"kn": 1, "tn": 352, "tiles_m": 8, "tiles_n": 4}
         # 671B up/gate: K = 7168 = 16 x 448 with the 256 side on A (N = 4096)
         assert mx.tile_config(32, 4096, 7168, 262144) == {"kn": 0, "tn": 448, "tiles_m": 16, "tiles_n": 16}
-        # 671B down: K = 2048 in 5 tiles of 416 (1.6% padding), the 256 side on A (N = 7168)
+        # 671B down: K = 2048 = 8 x 256 on the 256 side (B), N = 7168 = 16 x 448, every
+        # transposed chunk staged for a TMA store; forced onto A, 5 tiles of 416 (1.6% padding)
+        assert mx.tile_config(32, 7168, 2048, 524288) == {"kn": 1, "tn": 448, "tiles_m": 8, "tiles_n": 16}
+        mx.set_tile_orientation(1)
         assert mx.tile_config(32, 7168, 2048, 524288) == {"kn": 0, "tn": 416, "tiles_m": 28, "tiles_n": 5}
+        mx.set_tile_orientation(0)
         # many experts with 32 tokens each: bound by writing the output; the widest
         # tiles whose chunks are all written by staged TMA stores
         assert mx.tile_config(512, 512, 2048, 16384) == {"kn": 0, "tn": 448, "tiles_m": 2, "tiles_n": 5}
