@@ -247,7 +247,14 @@ __global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __rest
     const int nblk = mblocks + sn_side.tiles * sn_side.blocks;
     const long long ntasks = static_cast<long long>(nblk) * nchunks;
     const long long sM = M / 32;
-    for (long long task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    // On the grid block 0 builds only the plan (its scan of offs would
+    // otherwise delay its share of the gather: measured 4.1 against 3.3 us
+    // for the other blocks at the 16B shape); the other blocks gather.
+    const bool plan_only = grid && gridDim.x > 1;
+    const long long tstride = plan_only ? gridDim.x - 1 : gridDim.x;
+    for (long long task = plan_only ? static_cast<long long>(blockIdx.x) - 1 : blockIdx.x; task < ntasks;
+         task += tstride) {
+        if (task < 0) break;
         const int hb = static_cast<int>(task / nchunks);
         const int gs0 = static_cast<int>(task - static_cast<long long>(hb) * nchunks) * PREP_TILE_STEPS;
         const bool mside = hb < mblocks;
@@ -1499,11 +1506,15 @@ TileConfig best_of(int kn, int rows_m, int rows_n, double steps, int force_tn, b
 // 11-18 GB read per launch against 5 GB of operands, 7.2 GB with the
 // barrier). The barrier costs the idle time of the pairs that finish a pass
 // early, small only when a pass mostly holds one expert. Measured on GB300
-// with one call per variant: 671B down (140 tiles per expert, 15 pairs
-// sharing each N-side tile) +2.6% back to back; 671B up/gate (256 tiles, 4.75
-// pairs sharing each M-side stripe) -1%; 16B and 16B production (32 tiles
-// per expert, two or three experts per pass) -6% and -2.5%. On: at least one
-// pass of tiles per expert and at least 8 pairs sharing each far tile.
+// with one call per variant: 671B down on 28 x 5 tiles of 416 (140 tiles per
+// expert, 15 pairs sharing each N-side tile) +2.6% back to back; 671B down on
+// 16 x 8 tiles of 448 with the 256 side on B (128 tiles, 9.5 pairs sharing
+// each stripe of A) DRAM reads 7.4 -> 7.0 GB, main kernel +2.5% after L2
+// flushes and -1.2% back to back (two interleaved pairs of runs); 671B
+// up/gate (256 tiles, 4.75 pairs sharing each M-side stripe) -1%; 16B and
+// 16B production (32 tiles per expert, two or three experts per pass) -6%
+// and -2.5%. On: at least one pass of tiles per expert and at least 8 pairs
+// sharing each far tile.
 int use_pass_barrier(const TileConfig& tc, int G) {
     const long long ntpe = static_cast<long long>(tc.tiles_m) * tc.tiles_n;
     const int inner = tc.m_fastest ? tc.tiles_m : tc.tiles_n;
@@ -1617,7 +1628,7 @@ cudaError_t launch_wgrad(const WgradArgs& a, const CUtensorMap* maps, const char
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wgrad_prep, PREP_THREADS, sm);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) per_sm = 1;
-        long long blocks = tasks;
+        long long blocks = tasks + (a.grid ? 1 : 0);  // on the grid block 0 only plans
         if (blocks > static_cast<long long>(per_sm) * a.num_sms) blocks = static_cast<long long>(per_sm) * a.num_sms;
         if (blocks < 1) blocks = 1;
         // The L2 prefetch of the planes at the prep's entry pays while its
