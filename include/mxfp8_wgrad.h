@@ -108,7 +108,14 @@ size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M);
  * device pointer, 256-byte aligned, of at least
  * mxfp8_wgrad_workspace_bytes(E,N,K,M) bytes (else MXFP8_ENOWS). The
  * workspace must not be used by any other work until this call's kernels have
- * finished on `stream`. */
+ * finished on `stream`.
+ *
+ * This call allocates nothing, so it may be recorded by CUDA stream capture
+ * once the same sizes have been run eagerly in the context (which loads the
+ * kernels and sets their attributes): the graph holds its two kernel launches,
+ * and every replay reads the operands, scales and offs anew from the same
+ * buffers (tests/test_gpu_graph.py). mxfp8_wgrad_grouped may grow its cached
+ * scratch on a stream it has not seen, which stream capture does not allow. */
 int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                            const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
                            void* workspace, size_t workspace_bytes, void* stream);

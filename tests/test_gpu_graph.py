@@ -1,0 +1,112 @@
+"""The weight gradient captured in a CUDA graph and replayed.
+
+With a caller-provided workspace (mxfp8_wgrad_grouped_ws) a call allocates
+nothing, so its two launches (the plan / scale re-layout kernel, then the main
+kernel as its programmatic dependent, cooperative where the producers meet at
+expert boundaries) can be recorded in a graph. The graph reads the operands,
+scales and offs from the same device buffers on every replay, so new contents
+and a new routing copied into them are picked up. Checked: every replay gives
+the same bits as an eager call on the same inputs, the small case stays within
+the parity tolerance of the oracle, and the device status word stays clear."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_ragged_contraction_gb300 as mx
+
+from _util import quantised_operand, tolerance_violations
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mx.build()
+    mx.load()
+    mx.device_status(clear=True)
+
+
+def random_operand(rows, M, gen):
+    """E4M3 codes of magnitude at most 15 (no NaN bytes) with scales 2^-3 .. 2^3, generated on the GPU."""
+    mag = torch.randint(0, 0x58, (rows, M), dtype=torch.uint8, device="cuda", generator=gen)
+    sign = torch.randint(0, 2, (rows, M), dtype=torch.uint8, device="cuda", generator=gen) << 7
+    s = torch.randint(124, 131, (rows, M // 32), dtype=torch.uint8, device="cuda", generator=gen)
+    return mag | sign, s
+
+
+def routing(E, M, gen):
+    """Inclusive ends of E runs of 32-token multiples (some empty) covering at most M tokens."""
+    w = torch.rand(E, generator=gen, device="cuda").cpu().numpy() + 0.05
+    w[0] = 0.0                                   # one empty expert
+    sizes = np.floor(w / w.sum() * (M // 32)).astype(np.int64) * 32
+    return np.cumsum(sizes).astype(np.int32)
+
+
+def eager(A, sA, B, sB, offs, ws, E, N, K):
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    mx.wgrad_grouped(A, sA, B, sB, offs, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("E,N,K,M", [
+    (5, 384, 768, 3072),        # small: one or two passes, no pass barrier
+    (4, 7168, 2048, 65536),     # the 671B down expert shape: 128 tiles per expert, pass barrier on
+])
+def test_graph_replay_same_bits_as_eager(E, N, K, M):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(E * 1000 + N)
+    A, sA = random_operand(N, M, gen)
+    B, sB = random_operand(K, M, gen)
+    offs = torch.from_numpy(routing(E, M, gen)).cuda()
+    ws = torch.empty(mx.workspace_bytes(E, N, K, M), dtype=torch.uint8, device="cuda")
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+
+    mx.wgrad_grouped(A, sA, B, sB, offs, out=out, workspace=ws)  # attributes and module set up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.wgrad_grouped(A, sA, B, sB, offs, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert mx.device_status(clear=True) == 0
+
+    for rep in range(3):
+        if rep:
+            # new operand contents and a new routing in the same buffers
+            a2, s2 = random_operand(N, M, gen)
+            A.copy_(a2)
+            sA.copy_(s2)
+            offs.copy_(torch.from_numpy(routing(E, M, gen)).cuda())
+        out.view(torch.int16).fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert mx.device_status(clear=True) == 0
+        ref = eager(A, sA, B, sB, offs, ws, E, N, K)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"replay {rep} differs from the eager call"
+
+
+def test_graph_replay_matches_oracle():
+    E, N, K, M = 6, 256, 512, 2048
+    sizes = [32, 0, 704, 480, 96, 736]
+    A, sA = quantised_operand(N, M, seed=77, stream=0)
+    B, sB = quantised_operand(K, M, seed=77, stream=1)
+    offs = np.cumsum(sizes).astype(np.int32)
+    d = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (A, sA, B, sB, offs)]
+    ws = torch.empty(mx.workspace_bytes(E, N, K, M), dtype=torch.uint8, device="cuda")
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    mx.wgrad_grouped(*d, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.wgrad_grouped(*d, out=out, workspace=ws)
+    out.view(torch.int16).fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert mx.device_status(clear=True) == 0
+    bits = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref, _, aacc = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
+    assert not tolerance_violations(bits, ref, aacc).any()
+    assert not bits[1].any(), "empty expert not exact +0"
