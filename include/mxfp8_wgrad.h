@@ -92,7 +92,11 @@ extern "C" {
  * Scratch space (the scale re-layout and the schedule) comes from a cache the
  * library keeps per (device, stream), grown with stream-ordered allocation and
  * reused across calls; calls on one stream are ordered, so they never share
- * scratch concurrently.
+ * scratch concurrently. While `stream` is being captured into a CUDA graph the
+ * cache does not grow: a call needing more scratch than the stream already
+ * holds returns MXFP8_ENOWS (with a message) and records nothing, so make the
+ * same call once on that stream before capturing, or use
+ * mxfp8_wgrad_grouped_ws.
  */
 int mxfp8_wgrad_grouped(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                         const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
@@ -114,8 +118,7 @@ size_t mxfp8_wgrad_workspace_bytes(int E, int N, int K, int64_t M);
  * once the same sizes have been run eagerly in the context (which loads the
  * kernels and sets their attributes): the graph holds its two kernel launches,
  * and every replay reads the operands, scales and offs anew from the same
- * buffers (tests/test_gpu_graph.py). mxfp8_wgrad_grouped may grow its cached
- * scratch on a stream it has not seen, which stream capture does not allow. */
+ * buffers (tests/test_gpu_graph.py). */
 int mxfp8_wgrad_grouped_ws(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                            const int32_t* offs, int E, int N, int K, int64_t M, uint16_t* out,
                            void* workspace, size_t workspace_bytes, void* stream);

@@ -161,7 +161,11 @@ int make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t blocks, int box_b
 
 // Scratch cache keyed by (device, stream). Growth frees the old block in
 // stream order and allocates the new one in stream order, so earlier calls
-// on the same stream finish with the old block first.
+// on the same stream finish with the old block first. While the stream is
+// being captured into a CUDA graph the cache neither grows nor frees (a
+// captured allocation would belong to the graph, and the cache would keep a
+// pointer the graph owns): a call that needs more scratch than the stream's
+// cached block fails with MXFP8_ENOWS before anything is recorded.
 struct WsEntry {
     int dev;
     cudaStream_t stream;
@@ -171,6 +175,9 @@ struct WsEntry {
 std::vector<WsEntry> g_ws;
 
 int cached_workspace(int dev, cudaStream_t stream, size_t need, void** out) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t ec = cudaStreamIsCapturing(stream, &cap);
+    if (ec != cudaSuccess) return fail_cuda(ec, "cudaStreamIsCapturing");
     std::lock_guard<std::mutex> lk(g_mu);
     for (WsEntry& w : g_ws) {
         if (w.dev == dev && w.stream == stream) {
@@ -178,6 +185,17 @@ int cached_workspace(int dev, cudaStream_t stream, size_t need, void** out) {
                 *out = w.ptr;
                 return MXFP8_OK;
             }
+            break;
+        }
+    }
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(MXFP8_ENOWS,
+                    "the stream is being captured and the scratch cached for it holds less than the %zu bytes this "
+                    "call needs: pass a workspace (the _ws entry point) or make the same call once on this stream "
+                    "before capturing",
+                    need);
+    for (WsEntry& w : g_ws) {
+        if (w.dev == dev && w.stream == stream) {
             cudaError_t e = cudaFreeAsync(w.ptr, stream);
             if (e != cudaSuccess) return fail_cuda(e, "cudaFreeAsync (workspace)");
             w.ptr = nullptr;

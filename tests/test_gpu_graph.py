@@ -110,3 +110,38 @@ def test_graph_replay_matches_oracle():
     ref, _, aacc = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
     assert not tolerance_violations(bits, ref, aacc).any()
     assert not bits[1].any(), "empty expert not exact +0"
+
+
+def test_plain_entry_point_under_capture():
+    """The plain entry point's scratch cache does not allocate while its stream
+    is captured: a first call on a capturing stream fails with MXFP8_ENOWS and
+    records nothing; after the same call has run once eagerly on that stream,
+    capture reuses the cached scratch and replays give the eager bits."""
+    E, N, K, M = 3, 256, 512, 2048
+    sizes = [512, 0, 1504]
+    A, sA = quantised_operand(N, M, seed=78, stream=0)
+    B, sB = quantised_operand(K, M, seed=78, stream=1)
+    offs = np.cumsum(sizes).astype(np.int32)
+    d = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (A, sA, B, sB, offs)]
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    ref = mx.wgrad_grouped(*d)  # library state set up on the default stream
+    torch.cuda.synchronize()
+
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(mx.Mxfp8Error, match="being captured"):
+        with torch.cuda.graph(g, stream=s):
+            mx.wgrad_grouped(*d, out=out)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(s):
+        mx.wgrad_grouped(*d, out=out)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        mx.wgrad_grouped(*d, out=out)
+    out.view(torch.int16).fill_(-1)
+    g2.replay()
+    torch.cuda.synchronize()
+    assert mx.device_status(clear=True) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
