@@ -167,7 +167,8 @@ int mxfp8_quantize_tokenwise(const float* x, int R, int64_t M, uint8_t* q, uint8
  *   out  [M][N] bf16, 16-byte aligned; every element is written
  *
  * Scratch comes from the same per-(device, stream) cache as
- * mxfp8_wgrad_grouped. The tile width follows mxfp8_wgrad_set_tile_rows
+ * mxfp8_wgrad_grouped, with the same rule under stream capture (no growth
+ * while the stream is captured). The tile width follows mxfp8_wgrad_set_tile_rows
  * (the 256-row side is always on the rows of X).
  */
 int mxfp8_grouped_gemm(const uint8_t* X, const uint8_t* sX, const uint8_t* W, const uint8_t* sW,

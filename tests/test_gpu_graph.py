@@ -1,4 +1,4 @@
-"""The weight gradient captured in a CUDA graph and replayed.
+"""The library's calls captured in CUDA graphs and replayed.
 
 With a caller-provided workspace (mxfp8_wgrad_grouped_ws) a call allocates
 nothing, so its two launches (the plan / scale re-layout kernel, then the main
@@ -7,7 +7,10 @@ expert boundaries) can be recorded in a graph. The graph reads the operands,
 scales and offs from the same device buffers on every replay, so new contents
 and a new routing copied into them are picked up. Checked: every replay gives
 the same bits as an eager call on the same inputs, the small case stays within
-the parity tolerance of the oracle, and the device status word stays clear."""
+the parity tolerance of the oracle, and the device status word stays clear.
+The entry points that keep scratch per stream (mxfp8_wgrad_grouped,
+mxfp8_grouped_gemm) refuse to grow it while their stream is captured and are
+captured after one eager call on that stream."""
 import numpy as np
 import pytest
 import torch
@@ -145,3 +148,42 @@ def test_plain_entry_point_under_capture():
     torch.cuda.synchronize()
     assert mx.device_status(clear=True) == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_grouped_gemm_under_capture():
+    """The grouped GEMM with ragged rows (the layer's forward product) captured
+    after one eager call on the capturing stream: replays with new rows of X
+    and a new routing in the captured buffers give the eager bits, and rows
+    past the last group stay +0."""
+    E, M, N, K = 4, 1000, 384, 512
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4242)
+    X, sX = random_operand(M, K, gen)
+    W = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+    sW = torch.empty((E, N, K // 32), dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        W[e], sW[e] = random_operand(N, K, gen)
+    offs = torch.tensor([200, 200, 650, 960], dtype=torch.int32, device="cuda")  # an empty group, 40 padding rows
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        mx.grouped_gemm(X, sX, W, sW, offs, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.grouped_gemm(X, sX, W, sW, offs, out=out)
+    for rep in range(2):
+        if rep:
+            x2, s2 = random_operand(M, K, gen)
+            X.copy_(x2)
+            sX.copy_(s2)
+            offs.copy_(torch.tensor([96, 480, 480, 992], dtype=torch.int32, device="cuda"))
+        out.view(torch.int16).fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert mx.device_status(clear=True) == 0
+        ref = mx.grouped_gemm(X, sX, W, sW, offs)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"replay {rep} differs from the eager call"
+        last = int(offs[-1])
+        assert not out[last:].view(torch.int16).any(), "padding rows not +0"

@@ -11,7 +11,7 @@ mxfp8_wgrad_grouped_sf), through the C ABI.
   block products in the same order), for runs that start inside a 128-token
   step, empty experts and token padding, both tile orientations and several
   tile widths; and it is within the parity tolerance of the oracle.
-* At the 16B and 671B down shapes (full size, the library's own tiling) the
+* At the 16B, 671B down and 671B up/gate shapes (full size, the library's own tiling) the
   two entry points agree bit for bit over the whole output."""
 import numpy as np
 import pytest
@@ -129,7 +129,7 @@ def test_wgrad_sf_same_bits_as_regular(E, N, K, M, sizes, kn, tn):
         lo = int(offs[g])
 
 
-@pytest.mark.parametrize("name", ["16B", "671Bd"])
+@pytest.mark.parametrize("name", ["16B", "671Bd", "671Bgu"])
 def test_wgrad_sf_full_size(name):
     """Full-size operands generated on the GPU, quantised once with both the
     plane and the blocks for the library's own tiling: the two entry points
