@@ -1,0 +1,91 @@
+"""Randomised shapes and routings against the oracle (full outputs).
+
+Seeded draws of E, N, K, M and of the routing (empty experts, runs that start
+and end inside a 128-token step, tokens left past the last run), each under
+the library's own tiling and under a forced orientation and tile width, with
+realistic quantised operands. Every output element is compared with the
+oracle within the parity tolerance (NaN-poisoned outputs, so an unwritten
+element shows), empty experts are exact +0, and the forced tiling gives the
+same bits as the library's own (each output element sums the same 32-token
+block products in the same order whatever the tiling)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_ragged_contraction_gb300 as mx
+
+from _util import quantised_operand, tolerance_violations
+
+pytestmark = pytest.mark.gpu
+
+CASES = 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mx.build()
+    mx.load()
+    mx.device_status(clear=True)
+    yield
+    mx.set_tile_orientation(0)
+    mx.set_tile_rows(0)
+
+
+def draw_case(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 41))
+    N = int(rng.integers(1, 90)) * 8
+    K = int(rng.integers(1, 110)) * 8
+    M = int(rng.integers(1, 129)) * 32
+    # runs in 32-token units: some empty, the rest random, a random tail left unused
+    units = M // 32
+    used = int(rng.integers(units // 2, units + 1))
+    w = rng.random(E) * (rng.random(E) > 0.2)
+    if w.sum() == 0:
+        sizes = np.zeros(E, np.int64)
+    else:
+        sizes = np.floor(w / w.sum() * used).astype(np.int64)
+    offs = (np.cumsum(sizes) * 32).astype(np.int32)
+    # forced tiling for the second run: an orientation and an admissible width
+    orient = int(rng.integers(1, 3))
+    tn = int(rng.integers(1, 29)) * 16
+    return E, N, K, M, offs, orient, tn
+
+
+def run(A, sA, B, sB, offs, E, N, K):
+    d = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (A, sA, B, sB, offs)]
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+    out.view(torch.int16).fill_(-1)
+    mx.wgrad_grouped(*d, out=out)
+    torch.cuda.synchronize()
+    assert mx.device_status(clear=True) == 0
+    return out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_shape_against_oracle(seed):
+    E, N, K, M, offs, orient, tn = draw_case(1000 + seed)
+    A, sA = quantised_operand(N, M, seed=2000 + seed, stream=0, block_rows=64)
+    B, sB = quantised_operand(K, M, seed=2000 + seed, stream=1, block_rows=64)
+    try:
+        mx.set_tile_orientation(0)
+        mx.set_tile_rows(0)
+        got = run(A, sA, B, sB, offs, E, N, K)
+        mx.set_tile_orientation(orient)
+        mx.set_tile_rows(tn)
+        forced = run(A, sA, B, sB, offs, E, N, K)
+    finally:
+        mx.set_tile_orientation(0)
+        mx.set_tile_rows(0)
+    ref, _, aacc = oracle.wgrad(A, sA, B, sB, offs, E, N, K, M, want_acc=True)
+    bad = tolerance_violations(got, ref, aacc)
+    assert not bad.any(), f"E={E} N={N} K={K} M={M}: {bad.sum()} elements out of tolerance"
+    assert np.array_equal(got, forced), f"E={E} N={N} K={K} M={M}: orientation {orient}, tn {tn} gave other bits"
+    lo = 0
+    for g in range(E):
+        if int(offs[g]) == lo:
+            assert not got[g].any(), f"empty expert {g} not exact +0"
+        lo = int(offs[g])
