@@ -1,4 +1,5 @@
-"""Randomised shapes and routings against the oracle (full outputs).
+"""Randomised shapes and routings against the oracle (full outputs): the
+weight gradient and the grouped GEMM with ragged rows.
 
 Seeded draws of E, N, K, M and of the routing (empty experts, runs that start
 and end inside a 128-token step, tokens left past the last run), each under
@@ -89,3 +90,39 @@ def test_random_shape_against_oracle(seed):
         if int(offs[g]) == lo:
             assert not got[g].any(), f"empty expert {g} not exact +0"
         lo = int(offs[g])
+
+
+def draw_gemm_case(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 17))
+    M = int(rng.integers(1, 1500))
+    N = int(rng.integers(1, 80)) * 8
+    K = int(rng.integers(1, 25)) * 32
+    used = int(rng.integers(M // 2, M + 1))
+    w = rng.random(E) * (rng.random(E) > 0.2)
+    sizes = np.zeros(E, np.int64) if w.sum() == 0 else np.floor(w / w.sum() * used).astype(np.int64)
+    return E, M, N, K, np.cumsum(sizes).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_grouped_gemm_against_oracle(seed):
+    """The grouped GEMM with ragged rows (groups cut at any row) on random
+    shapes: within the parity tolerance of the oracle, rows past the last group
+    exact +0."""
+    E, M, N, K, offs = draw_gemm_case(3000 + seed)
+    X, sX = quantised_operand(M, K, seed=4000 + seed, stream=0, block_rows=16)
+    W = np.empty((E, N, K), np.uint8)
+    sW = np.empty((E, N, K // 32), np.uint8)
+    for e in range(E):
+        W[e], sW[e] = quantised_operand(N, K, seed=5000 + seed, stream=1 + e, block_rows=16)
+    d = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (X, sX, W, sW, offs)]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    out.view(torch.int16).fill_(-1)
+    mx.grouped_gemm(*d, out=out)
+    torch.cuda.synchronize()
+    assert mx.device_status(clear=True) == 0
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref, _, aacc = oracle.grouped_gemm(X, sX, W, sW, offs, E, M, N, K, want_acc=True)
+    bad = tolerance_violations(got, ref, aacc)
+    assert not bad.any(), f"E={E} M={M} N={N} K={K}: {bad.sum()} elements out of tolerance"
+    assert not got[int(offs[-1]):].any(), "rows past the last group not +0"
