@@ -1,5 +1,6 @@
 """Randomised shapes and routings against the oracle (full outputs): the
-weight gradient and the grouped GEMM with ragged rows.
+weight gradient, the grouped GEMM with ragged rows, and the path over scale
+blocks written by the quantiser (against the regular path's bits).
 
 Seeded draws of E, N, K, M and of the routing (empty experts, runs that start
 and end inside a 128-token step, tokens left past the last run), each under
@@ -126,3 +127,42 @@ def test_random_grouped_gemm_against_oracle(seed):
     bad = tolerance_violations(got, ref, aacc)
     assert not bad.any(), f"E={E} M={M} N={N} K={K}: {bad.sum()} elements out of tolerance"
     assert not got[int(offs[-1]):].any(), "rows past the last group not +0"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_scale_block_path_same_bits(seed):
+    """The quantiser that writes scale-factor blocks and the weight gradient
+    over them (mxfp8_quantize_transpose_bf16_sf, mxfp8_wgrad_grouped_sf) on
+    random shapes and routings, for the library's tiling and for a random
+    other one: the regular entry point's bits on the same quantised operands."""
+    rng = np.random.default_rng(6000 + seed)
+    E = int(rng.integers(1, 25))
+    N = int(rng.integers(1, 700))
+    K = int(rng.integers(1, 90)) * 8
+    M = int(rng.integers(1, 97)) * 32
+    units = M // 32
+    used = int(rng.integers(units // 2, units + 1))
+    w = rng.random(E) * (rng.random(E) > 0.2)
+    sizes = np.zeros(E, np.int64) if w.sum() == 0 else np.floor(w / w.sum() * used).astype(np.int64)
+    offs = torch.from_numpy((np.cumsum(sizes) * 32).astype(np.int32)).cuda()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7000 + seed)
+    dy = torch.randn(M, N, device="cuda", generator=g).to(torch.bfloat16)
+    x = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    cfg = mx.tile_config(E, N, K, M)
+    tilings = [(cfg["kn"], cfg["tn"]), (int(rng.integers(0, 2)), int(rng.integers(1, 29)) * 16)]
+    ref = None
+    for kn, tn in tilings:
+        sA = torch.empty((N, M // 32), dtype=torch.uint8, device="cuda")
+        sB = torch.empty((K, M // 32), dtype=torch.uint8, device="cuda")
+        A, sfA, _ = mx.quantize_transpose_bf16_sf(dy, tn if kn else 256, s=sA)
+        B, sfB, _ = mx.quantize_transpose_bf16_sf(x, 256 if kn else tn, s=sB)
+        if ref is None:
+            ref = mx.wgrad_grouped(A, sA, B, sB, offs)
+        got = torch.empty_like(ref)
+        got.view(torch.int16).fill_(-1)
+        mx.wgrad_grouped_sf(A, sfA, B, sfB, offs, kn, tn, out=got)
+        torch.cuda.synchronize()
+        assert mx.device_status(clear=True) == 0
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), \
+            f"E={E} N={N} K={K} M={M} kn={kn} tn={tn}: not the regular entry point's bits"
