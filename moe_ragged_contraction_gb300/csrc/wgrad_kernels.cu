@@ -124,9 +124,7 @@ __device__ __forceinline__ uint32_t load_scale4_edge(const uint8_t* __restrict__
 // zero past the tile or the plane), and row r, 32-token block kb sits at byte
 // (r % 32) * 16 + (r / 32) * 4 + kb. Blocks: the M side's tiles * blocks
 // first, then the N side's.
-// (at most 32 registers a thread, so that eight blocks share an SM: the
-// gathers' loads in flight set its speed)
-__global__ void __launch_bounds__(PREP_THREADS, 8) wgrad_prep(const int32_t* __restrict__ offs, const PrepSide sm_side,
+__global__ void __launch_bounds__(PREP_THREADS) wgrad_prep(const int32_t* __restrict__ offs, const PrepSide sm_side,
                                                            const PrepSide sn_side, int32_t* __restrict__ plan, int E,
                                                            long long M, int ts_max, int grid, int prefetch) {
     extern __shared__ int prep_smem[];
